@@ -1,0 +1,401 @@
+"""Benchmark of the CP lookup-decode on GB300: rows/s and achieved HBM GB/s.
+
+A step is one cp_lookup_decode over the whole replay batch (default: the
+DeepSeek-scale table, 1.98e8 rows x d=1024 at b=2 = 51 GB of records in HBM,
+4096 tokens x 48 rows = 196,608 Zipf(1.0) lookups).  W untimed warm-up steps,
+then K timed steps; each step is bracketed by CUDA events on the launching
+stream and followed (outside the timed interval) by a 512 MB write that flushes
+the 129 MB L2, so no step reuses the previous step's records from L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--layout aos|soa] [--host-path]
+
+Under torchrun (N > 1) every rank holds its own replica of the table and
+decodes its own replay (seed + rank); no collective touches the data path
+(weak scaling).  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain C++ restatement of the
+method, test infrastructure) on this machine's host cores over bounded samples
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+FALLBACK_HBM_GBS = 6800.0       # earlier GB300 copy measurement, used when no measured file
+PAGES_LATENCY_S = 0.190e-3      # pages' HBM-resident replay latency on one H200
+L2_FLUSH_BYTES = 512 << 20
+METRIC = "CP lookup-decode rows/s & achieved HBM GB/s, 4096-tok×48-row replay"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="deepseek_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layout", default="aos", choices=["aos", "soa"])
+    ap.add_argument("--host-path", action="store_true",
+                    help="also time cp_lookup_decode_host on the table in pinned host DRAM")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            j = json.loads(p.read_text())
+            for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if key in j and isinstance(j[key], (int, float)):
+                    return float(j[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "trellis_row_decode_gb300" / "csrc").glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str, layout: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
+    p = ROOT / "profiles" / "ncu_traffic.json"
+    if not p.exists():
+        return None
+    try:
+        j = json.loads(p.read_text())
+    except Exception:
+        return None
+    for e in j.get("entries", []):
+        if e.get("workload") == workload and e.get("layout") == layout and \
+                e.get("kernel_source_sha256") == kernel_source_sha():
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.2)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(self.out or "")):
+            if len(r) >= 9:
+                rows.append([x.strip() for x in r])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": float(np.median(loaded)) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the host cores.
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut):
+    """Oracle lookup-decode rows/s on a bounded prefix of the replay, all host cores."""
+    import torch
+    import oracle
+    from trellis_row_decode_gb300 import synth
+    nt = max(1, os.cpu_count() or 1)
+    # calibrate on a short prefix, then time a prefix sized for `seconds`
+    def run(m):
+        sub = idx[:m]
+        uniq, inv = np.unique(sub, return_inverse=True)
+        rec = synth.gen_records(synth.SEED_TABLE, torch.from_numpy(uniq), w.d, w.k).numpy()
+        t0 = time.perf_counter()
+        oracle.lookup_decode(rec, len(uniq), w.d, w.k, rec.shape[1], lut, inv.astype(np.int64),
+                             n_threads=nt)
+        return time.perf_counter() - t0
+    m0 = min(idx.size, 2048)
+    dt0 = run(m0)
+    m = int(min(idx.size, max(m0, m0 * seconds / max(dt0, 1e-6))))
+    dt = run(m)
+    return m / dt, m, nt
+
+
+def reference_arm(args, w, rank):
+    if rank != 0:
+        return
+    import trellis_row_decode_gb300 as cp
+    lut = cp.default_lut()
+    idx = w.indices()
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    per_step = min(per_step, 10.0)
+    rates, sizes, nt = [], [], 1
+    for s in range(args.warmup + args.steps):
+        rate, m, nt = oracle_sample_rate(w, idx, per_step, lut)
+        if s >= args.warmup:
+            rates.append(rate)
+            sizes.append(m)
+    value = float(np.median(rates))
+    bpl = w.algorithmic_bytes_per_lookup()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w.n_lookups / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
+                   "lookups": w.n_lookups, "index_dist": f"{w.dist}({w.zipf_s})"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nt, "kind": "oracle",
+                         "sample": f"first {sizes[0]} lookups of the replay per step, "
+                                   f"records regenerated on the host, {nt} threads"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "achieved_gbs_algorithmic": value * bpl / 1e9,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Our arm.
+# ---------------------------------------------------------------------------
+
+def build_table(w, layout: str, seed: int):
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    rec = torch.empty(w.table_bytes, dtype=torch.uint8, device="cuda")
+    synth.fill_records(rec, seed, w.n_rows, w.d, w.k)
+    soa = None
+    lay = cp.CP_LAYOUT_AOS
+    if layout == "soa":
+        soa = torch.empty(cp.soa_bytes(w.n_rows, w.d, w.k), dtype=torch.uint8, device="cuda")
+        lay = cp.CP_LAYOUT_SOA
+    table = cp.load_table(rec, w.n_rows, w.d, w.k, cp.default_lut(), layout=lay, soa=soa)
+    torch.cuda.synchronize()
+    return table, rec, soa
+
+
+def time_steps(fn, steps, warmup, flush, stream):
+    """Per-step device times (s) of fn() with an L2 flush between steps."""
+    import torch
+    for _ in range(warmup):
+        fn()
+        flush.zero_()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
+
+
+def our_arm(args, w, rank, world, local):
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    table, rec, soa = build_table(w, args.layout, synth.SEED_TABLE)
+    idx_np = w.indices(synth.SEED_INDEX + rank)
+    idx = torch.from_numpy(idx_np).cuda()
+    n = idx_np.size
+    out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    step = lambda: cp.lookup_decode(table, idx, out, stream)  # noqa: E731
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t = time_steps(step, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    status = cp.get_status(table)
+    assert status == cp.CP_OK, status
+    total = float(t.sum())
+    if dist is not None:
+        tt = torch.tensor([total], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total = float(tt.item())
+    value = n * args.steps * world / total
+    mean_t = total / args.steps
+    bpl = w.algorithmic_bytes_per_lookup()
+    achieved = n * bpl / float(t.mean()) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # End to end through the public API: ids from pinned host memory, rows back
+    # to pinned host memory, both copies inside the timed region.
+    idx_h = torch.from_numpy(idx_np).pin_memory()
+    out_h = torch.empty((n, w.d), dtype=torch.bfloat16, pin_memory=True)
+    idx_d = torch.empty_like(idx)
+
+    def e2e_step():
+        idx_d.copy_(idx_h, non_blocking=True)
+        cp.lookup_decode(table, idx_d, out, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream)
+    e2e_value = n / float(te.mean())
+
+    host_obj = None
+    if args.host_path:
+        host_obj = host_path_measure(args, w, idx, flush, stream)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, m, nt = oracle_sample_rate(w, idx_np, args.cpu_seconds, cp.default_lut())
+        cpu = {"value": rate, "unit": "rows/s", "cores": nt, "kind": "oracle",
+               "sample": f"first {m} lookups of the replay, records regenerated on the host, "
+                         f"{nt} threads"}
+
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_t * 1e3,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / world / (w.n_lookups / PAGES_LATENCY_S)
+            if w.name == "deepseek_prefill" else None,
+            "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
+                       "record_bytes": w.rec_bytes, "lookups": n, "tokens": w.tokens,
+                       "rows_per_token": w.rows_per_token,
+                       "index_dist": f"{w.dist}({w.zipf_s})", "layout": args.layout,
+                       "table_gb": w.table_bytes / 1e9,
+                       "l2": "flushed between steps (512 MB write, outside the timed interval)",
+                       "parallelism": f"replicas x{world}"},
+            "achieved_gbs_algorithmic": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": ncu_traffic(w.name, args.layout),
+                         "bytes_per_lookup": bpl, "kernel": "lookup_decode_kernel"},
+            "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": n * 8,
+                    "d2h_bytes_per_step": n * w.d * 2},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+            "step_ms": {"min": float(t.min() * 1e3), "median": float(np.median(t) * 1e3),
+                        "max": float(t.max() * 1e3)},
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if host_obj is not None:
+            line["host_path"] = host_obj
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def host_path_measure(args, w, idx, flush, stream):
+    """cp_lookup_decode_host on the same table in pinned host DRAM, against measured H2D."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    R = w.rec_bytes
+    host = torch.empty(w.table_bytes, dtype=torch.uint8, pin_memory=True)
+    chunk = 1 << 22
+    stage = torch.empty(chunk * R, dtype=torch.uint8, device="cuda")
+    for r0 in range(0, w.n_rows, chunk):
+        r1 = min(w.n_rows, r0 + chunk)
+        rows = torch.arange(r0, r1, dtype=torch.int64, device="cuda")
+        stage[: (r1 - r0) * R].view(r1 - r0, R).copy_(
+            synth.gen_records(synth.SEED_TABLE, rows, w.d, w.k))
+        host[r0 * R: r1 * R].copy_(stage[: (r1 - r0) * R])
+    torch.cuda.synchronize()
+    # measured host-to-device bandwidth: 1 GB copies from pinned memory
+    dst = stage[: 1 << 30]
+    src = host[: 1 << 30]
+    th = time_steps(lambda: dst.copy_(src, non_blocking=True), 10, 2, flush, stream)
+    h2d = (1 << 30) / float(np.median(th)) / 1e9
+    del stage, dst
+    table = cp.load_table(host, w.n_rows, w.d, w.k, cp.default_lut())
+    n = idx.numel()
+    out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), 20, 3, flush, stream)
+    assert cp.get_status(table) == cp.CP_OK
+    link_gbs = n * R / float(np.median(t)) / 1e9
+    table.close()
+    return {"ms_per_step": float(np.median(t) * 1e3), "rows_per_s": n / float(np.median(t)),
+            "record_gbs": link_gbs, "h2d_measured_gbs": h2d, "frac_of_h2d": link_gbs / h2d}
+
+
+def main():
+    args = parse()
+    from trellis_row_decode_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        reference_arm(args, w, rank)
+        return
+    our_arm(args, w, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * cp.h -- C ABI of libcp, the GB300 (sm_103a) lookup-decode for Conditional
+ * Program (CP) compressed memory tables.
+ *
+ * Method (pages cited by title):
+ *   [P4] "2비트 코드와 공유 트렐리스로 n-gram 룩업 테이블을 4~8배 압축한다"
+ *        (onedev.kr/papers/1189)
+ *   [P1] "Two-bit lookup tables shrink DeepSeek's 203 GB memory to 51 GB and
+ *        cut prefill from 64.66 s to 13.27 s" (ai4snews.wisdomeyes.cn)
+ *
+ * Each table row i is one independently addressable record holding a b-bit-per-
+ * coordinate code c_i and a 16-bit scale alpha_i, b + 16/d bits per parameter;
+ * the reconstruction rule f is shared by the whole table and applied only to
+ * rows that are looked up: e_hat_i = alpha_i * f(c_i) [P4 section 어떻게 동작하나
+ * "how it works"].  The runtime fetches only the requested records, restores
+ * them with a fused kernel and hands them over in the original lookup order
+ * [P4 section 무엇과 다른가 "how it differs"].  The table can sit in GPU HBM or
+ * in pinned host DRAM read over the host link [P4 section 전제와 한계
+ * "assumptions and limits"; P1 "Interpretation"].
+ *
+ * Format constants (the pages leave them open; fixed here once):
+ *   V = 2 coordinates per trellis step; k = 2b bits per step, k in {3,4,5,6}
+ *   (b = 1.5, 2, 2.5, 3); T = d/2 steps; Lc = k*T code bits per row.
+ *   Code bit j = (code[j >> 3] >> (j & 7)) & 1 (LSB first, little-endian bytes).
+ *   State s_t = the 16 code bits ending at bit k(t+1), oldest bit lowest, bit
+ *   positions taken mod Lc (tail-biting).
+ *   h = s*s + s (mod 2^32); (y0, y1) = LUT[(h >> 14) & 511]; y1 = -y1 when bit
+ *   23 of h is set.  LUT: 512 fp16 pairs, shared by the table.
+ *   out[2t] = bf16_rn(float(alpha) * y0), out[2t+1] = bf16_rn(float(alpha) * y1):
+ *   one fp32 product (exact), one round-to-nearest-even to bf16.
+ *
+ * Record (AoS) layout, R = d*k/16 + 2 bytes, no padding:
+ *   [ code: d*k/16 bytes ][ alpha: bf16, little-endian ]
+ * Record i starts at byte i*R of the records buffer (2-byte aligned in general).
+ *
+ * Conventions for every call:
+ *   - Stream-ordered and asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  No call synchronises except cp_get_status.
+ *   - Argument errors are detected on the host and returned before any work is
+ *     queued; nothing is written in that case.
+ *   - The caller owns every large buffer (records, SoA copy, ids, output); a
+ *     table handle borrows them and they must outlive it.  The handle owns only
+ *     its LUT copy, its device status word and its geometry.
+ *   - Out-of-range ids never fault: the output row is written as zeros and the
+ *     table's device status word records CP_ERR_INDEX_OOB for cp_get_status.
+ *   - n = 0 is a valid no-op.
+ *   - Geometry accepted by the CUDA path: d % 8 == 0, 8 <= d <= 4096,
+ *     (d*k) % 32 == 0 (a record is a whole number of 16-bit words, so every
+ *     record starts 2-byte aligned), 1 <= n_rows <= 2^40.
+ */
+#ifndef CP_H_
+#define CP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct cp_table cp_table; /* opaque handle */
+
+typedef enum cp_status {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1, /* bad pointer, alignment, geometry or residency */
+  CP_ERR_INDEX_OOB = 2,   /* a previous decode saw an id outside [0, n_rows) */
+  CP_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  CP_ERR_NO_MEMORY = 4,   /* the handle's own small allocations failed */
+  CP_ERR_FORMAT = 5       /* LUT or record contents unusable (non-finite LUT) */
+} cp_status;
+
+enum { CP_LAYOUT_AOS = 0, CP_LAYOUT_SOA = 1 };
+enum { CP_RESIDENT_DEVICE = 0, CP_RESIDENT_HOST = 1 };
+
+/* Bytes of one AoS record: d*k/16 code bytes + 2 (the bf16 scale); this is
+ * exactly b + 16/d bits per parameter [P4 "how it works"].  0 if the geometry
+ * is not accepted. */
+uint64_t cp_record_bytes(uint32_t d, uint32_t bits_per_step);
+
+/* Bytes a caller must provide for the SoA copy of an n_rows table:
+ * codes[n_rows][S] with S = d*k/16 rounded up to 16, then alpha[n_rows] (bf16),
+ * the alpha array starting at byte n_rows*S and padded to a multiple of 16.
+ * 0 if the geometry is not accepted. */
+uint64_t cp_soa_bytes(uint64_t n_rows, uint32_t d, uint32_t bits_per_step);
+
+/*
+ * cp_table_load -- bind a compressed table (records in the AoS layout above)
+ * to a handle, validate its geometry, copy the shared LUT to the device and,
+ * for CP_LAYOUT_SOA, repack the records on the device into `soa_dst`.
+ *
+ *   out           receives the handle (set to NULL on error).
+ *   records       AoS records, n_rows * R bytes, 16-byte aligned.
+ *                 CP_RESIDENT_DEVICE: device memory.
+ *                 CP_RESIDENT_HOST: host memory, page-locked by the caller
+ *                 (cudaHostAlloc, or cudaHostRegister).  If it is plain pageable
+ *                 memory, the call registers it (mapped, read-only) and the
+ *                 handle unregisters it in cp_table_free.
+ *   n_rows, d, bits_per_step: the geometry (k = 2b).
+ *   lut_fp16      host pointer to 512 x (y0, y1) fp16 bit patterns (2048 bytes),
+ *                 copied during the call; every entry must be finite.
+ *   residency     CP_RESIDENT_DEVICE or CP_RESIDENT_HOST.
+ *   layout        CP_LAYOUT_AOS: the decoder reads `records` in place.
+ *                 CP_LAYOUT_SOA: the decoder reads `soa_dst` (cp_soa_bytes
+ *                 bytes, 16-byte aligned, device memory, or for a host-resident
+ *                 table pinned host memory) which this call fills, stream-ordered.
+ *   soa_dst       NULL for CP_LAYOUT_AOS.
+ *   stream        cudaStream_t for the LUT copy and the repack.
+ * The handle is usable by later work on `stream` (or on any stream after it has
+ * been synchronised).
+ */
+cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, uint32_t d,
+                        uint32_t bits_per_step, const uint16_t* lut_fp16, int residency,
+                        int layout, void* soa_dst, void* stream);
+
+/*
+ * cp_lookup_decode -- e_hat_j = alpha_{r_j} * f(c_{r_j}) for the n requested
+ * row ids r_j = idx[j], written as bf16 rows in lookup order, duplicates
+ * included [P4 "how it differs"].  The table must be CP_RESIDENT_DEVICE.
+ *
+ *   idx   device pointer, n int64 row ids, 8-byte aligned.
+ *   out   device pointer, bf16 [n][d] row-major (n*d*2 bytes), 16-byte aligned.
+ * Out-of-range ids give zero rows and set the status word (see cp_get_status).
+ */
+cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                           void* stream);
+
+/*
+ * cp_lookup_decode_host -- the same operation for a CP_RESIDENT_HOST table: the
+ * kernel reads only the requested records directly from pinned host DRAM over
+ * the host link (zero-copy) [P4 "assumptions and limits"; P1 "Interpretation"].
+ * idx and out are device pointers as for cp_lookup_decode.
+ */
+cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t n,
+                                uint16_t* out, void* stream);
+
+/*
+ * cp_get_status -- synchronise `stream`, then report and clear the table's
+ * device status word: CP_ERR_INDEX_OOB if any decode since the last call saw an
+ * out-of-range id, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK.
+ */
+cp_status cp_get_status(const cp_table* t, void* stream);
+
+/* Release what the handle owns (LUT copy, status word, host registration made
+ * by cp_table_load).  Borrowed buffers are untouched.  NULL is a no-op. */
+void cp_table_free(cp_table* t);
+
+/* Static string for a status code. */
+const char* cp_status_string(cp_status s);
+
+/* Text of the last CUDA error seen by this library on the calling thread ("" if
+ * none). */
+const char* cp_last_error(void);
+
+/* Test hook for failure handling on the host: the next `count` calls of the
+ * chosen kind fail as if the CUDA runtime had refused them
+ * (1 = device allocation, 2 = host registration / device alias).  Returns
+ * CP_ERR_INVALID_ARG for an unknown kind. */
+cp_status cp_test_inject_failure(int kind, int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_H_ */

@@ -1,0 +1,181 @@
+"""Python binding of libcp, the GB300 (sm_103a) CP lookup-decode.
+
+Argument marshalling only: every step of the decode runs in the CUDA kernels of
+libcp.so (built in-tree by ``trellis_row_decode_gb300.build_ext``).  PyTorch is
+used for device memory and streams.  There is no CPU fallback: if libcp.so is
+missing or fails to load, every call raises.
+
+The operations (pages cited by title, [P4] "2비트 코드와 공유 트렐리스로 n-gram
+룩업 테이블을 4~8배 압축한다"): a table row is an independently addressable
+record (code c_i, bf16 scale alpha_i); looking up ids r_j returns
+e_hat_j = alpha_{r_j} * f(c_{r_j}) as bf16 rows in lookup order [P4 sections
+어떻게 동작하나 and 무엇과 다른가].  The C ABI is declared in include/cp.h.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from pathlib import Path
+
+import numpy as np
+import torch
+
+__all__ = [
+    "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
+    "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH",
+    "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
+]
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_build" / "libcp.so"
+LUT_PATH = _PKG / "data" / "cp_lut_v2_l16_512.bin"
+
+CP_OK, CP_ERR_INVALID_ARG, CP_ERR_INDEX_OOB, CP_ERR_CUDA, CP_ERR_NO_MEMORY, CP_ERR_FORMAT = range(6)
+CP_LAYOUT_AOS, CP_LAYOUT_SOA = 0, 1
+CP_RESIDENT_DEVICE, CP_RESIDENT_HOST = 0, 1
+
+_lib = None
+
+
+class CPError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib.cp_status_string(status).decode() if _lib else str(status)
+        detail = _lib.cp_last_error().decode() if _lib else ""
+        super().__init__(f"{what}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+def lib():
+    """The loaded libcp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"libcp.so not built at {LIB_PATH}; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(str(LIB_PATH))
+        vp, u64, u32, i32 = C.c_void_p, C.c_uint64, C.c_uint32, C.c_int
+        L.cp_record_bytes.restype = u64
+        L.cp_record_bytes.argtypes = [u32, u32]
+        L.cp_soa_bytes.restype = u64
+        L.cp_soa_bytes.argtypes = [u64, u32, u32]
+        L.cp_table_load.restype = i32
+        L.cp_table_load.argtypes = [C.POINTER(vp), vp, u64, u32, u32, vp, i32, i32, vp, vp]
+        L.cp_lookup_decode.restype = i32
+        L.cp_lookup_decode.argtypes = [vp, vp, u64, vp, vp]
+        L.cp_lookup_decode_host.restype = i32
+        L.cp_lookup_decode_host.argtypes = [vp, vp, u64, vp, vp]
+        L.cp_get_status.restype = i32
+        L.cp_get_status.argtypes = [vp, vp]
+        L.cp_table_free.restype = None
+        L.cp_table_free.argtypes = [vp]
+        L.cp_status_string.restype = C.c_char_p
+        L.cp_status_string.argtypes = [i32]
+        L.cp_last_error.restype = C.c_char_p
+        L.cp_last_error.argtypes = []
+        L.cp_test_inject_failure.restype = i32
+        L.cp_test_inject_failure.argtypes = [i32, i32]
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != CP_OK:
+        raise CPError(status, what)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def record_bytes(d: int, k: int) -> int:
+    return int(lib().cp_record_bytes(d, k))
+
+
+def soa_bytes(n_rows: int, d: int, k: int) -> int:
+    return int(lib().cp_soa_bytes(n_rows, d, k))
+
+
+def default_lut() -> np.ndarray:
+    """The shared fp16 LUT (512 x (y0, y1) bit patterns) of this format."""
+    return np.fromfile(LUT_PATH, dtype="<u2").reshape(512, 2)
+
+
+class Table:
+    """A loaded compressed table.  Borrows `records` (and `soa`); keeps them alive."""
+
+    def __init__(self, handle: int, n_rows: int, d: int, k: int, residency: int, layout: int,
+                 keepalive: tuple):
+        self.handle = handle
+        self.n_rows, self.d, self.k = n_rows, d, k
+        self.residency, self.layout = residency, layout
+        self._keepalive = keepalive
+
+    def close(self) -> None:
+        if self.handle:
+            lib().cp_table_free(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def load_table(records: torch.Tensor, n_rows: int, d: int, k: int, lut: np.ndarray | None = None,
+               layout: int = CP_LAYOUT_AOS, soa: torch.Tensor | None = None,
+               stream=None) -> Table:
+    """Bind AoS records (uint8, device tensor or pinned host tensor) to a handle.
+
+    Residency follows the tensor: CUDA -> CP_RESIDENT_DEVICE, CPU -> CP_RESIDENT_HOST.
+    For layout=CP_LAYOUT_SOA pass `soa` (uint8, soa_bytes(n_rows, d, k) bytes) to
+    receive the on-device repack.
+    """
+    L = lib()
+    if records.dtype != torch.uint8 or not records.is_contiguous():
+        raise ValueError("records must be a contiguous uint8 tensor")
+    residency = CP_RESIDENT_DEVICE if records.is_cuda else CP_RESIDENT_HOST
+    if lut is None:
+        lut = default_lut()
+    lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    h = C.c_void_p(0)
+    soa_ptr = None
+    if layout == CP_LAYOUT_SOA:
+        if soa is None:
+            raise ValueError("CP_LAYOUT_SOA needs the soa buffer")
+        soa_ptr = soa.data_ptr()
+    st = L.cp_table_load(C.byref(h), records.data_ptr(), n_rows, d, k,
+                         lut.ctypes.data, residency, layout, soa_ptr, _stream_ptr(stream))
+    _check(st, "cp_table_load")
+    return Table(h.value, n_rows, d, k, residency, layout, (records, soa, lut))
+
+
+def _decode(fn, table: Table, idx: torch.Tensor, out: torch.Tensor | None, stream, what: str):
+    if idx.dtype != torch.int64 or not idx.is_cuda or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int64 CUDA tensor")
+    n = idx.numel()
+    if out is None:
+        out = torch.empty((n, table.d), dtype=torch.bfloat16, device=idx.device)
+    elif out.dtype != torch.bfloat16 or out.shape != (n, table.d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of shape (n, d)")
+    _check(fn(table.handle, idx.data_ptr(), n, out.data_ptr(), _stream_ptr(stream)), what)
+    return out
+
+
+def lookup_decode(table: Table, idx: torch.Tensor, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """bf16 [n, d] rows alpha_r * f(c_r) for r = idx[j], in lookup order (HBM-resident table)."""
+    return _decode(lib().cp_lookup_decode, table, idx, out, stream, "cp_lookup_decode")
+
+
+def lookup_decode_host(table: Table, idx: torch.Tensor, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Same as lookup_decode for a table resident in pinned host memory (zero-copy reads)."""
+    return _decode(lib().cp_lookup_decode_host, table, idx, out, stream,
+                   "cp_lookup_decode_host")
+
+
+def get_status(table: Table, stream=None) -> int:
+    """Synchronise the stream; CP_ERR_INDEX_OOB if an id was out of range since the last call."""
+    return int(lib().cp_get_status(table.handle, _stream_ptr(stream)))

@@ -1,0 +1,385 @@
+// cp_api.cu -- host side of libcp: validation, table handles, launches.
+// The operations are specified in include/cp.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "cp.h"
+#include "cp_dispatch.h"
+
+struct cp_table {
+  int device;
+  int residency;
+  int layout;
+  uint64_t n_rows;
+  uint32_t d;
+  uint32_t k;
+  uint32_t rec_bytes;     // R
+  uint32_t code_bytes;    // d*k/16
+  uint32_t soa_stride;    // S
+  const uint8_t* rec;     // device-accessible AoS records (HBM, or alias of host memory)
+  const uint8_t* soa_codes;
+  const uint16_t* soa_alpha;
+  uint32_t* lut_dev;      // 512 words
+  uint32_t* status_dev;   // 1 word
+  void* registered;       // host range this handle registered, else nullptr
+  int sm_count;
+  int max_smem;           // opt-in shared memory per block
+  cpk::KernelSet kernels;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<int> g_fail_alloc{0};
+std::atomic<int> g_fail_register{0};
+
+constexpr uint64_t kMaxRows = 1ull << 40;
+constexpr uint64_t kMaxLookups = 1ull << 40;
+
+cp_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return CP_ERR_CUDA;
+}
+
+bool take_injected(std::atomic<int>& c) {
+  int v = c.load();
+  while (v > 0) {
+    if (c.compare_exchange_weak(v, v - 1)) return true;
+  }
+  return false;
+}
+
+bool geometry_ok(uint32_t d, uint32_t k) {
+  if (k < 3 || k > 6) return false;
+  if (d < 8 || d > 4096 || (d % 8) != 0) return false;
+  // whole 16-bit words per record, so every record starts 2-byte aligned
+  if ((static_cast<uint64_t>(d) * k) % 32 != 0) return false;
+  return true;
+}
+
+uint32_t soa_stride(uint32_t d, uint32_t k) { return ((d * k / 16) + 15u) & ~15u; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cpk::KernelSet kernels_for(uint32_t k) {
+  switch (k) {
+    case 3: return cpk::kernels_k3();
+    case 4: return cpk::kernels_k4();
+    case 5: return cpk::kernels_k5();
+    default: return cpk::kernels_k6();
+  }
+}
+
+// Stage size in bytes for a geometry: the 16-byte aligned span that holds the
+// record (misalignment <= 14 bytes for AoS), plus 16 bytes of slack for the
+// 64-bit funnel reads past the code; SoA adds the 4-byte alpha slot.
+uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot) {
+  if (soa) {
+    *alpha_slot = t->soa_stride + 8;
+    return t->soa_stride + 16;
+  }
+  *alpha_slot = 0;
+  const uint32_t span = t->code_bytes + 2 + 14;
+  return ((span + 15u) & ~15u) + 16u;
+}
+
+cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                        cudaStream_t stream, bool host_path) {
+  const bool soa = (t->layout == CP_LAYOUT_SOA);
+  const int pf = host_path ? cpk::kPfHost : cpk::kPfDevice;
+  cpk::DecodeFn fn = host_path ? (soa ? t->kernels.soa_host : t->kernels.aos_host)
+                               : (soa ? t->kernels.soa_dev : t->kernels.aos_dev);
+  cpk::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = soa ? t->soa_codes : t->rec;
+  p.alpha = soa ? t->soa_alpha : nullptr;
+  p.n_rows = t->n_rows;
+  p.table_bytes = soa ? t->n_rows * t->soa_stride : t->n_rows * t->rec_bytes;
+  p.d = t->d;
+  p.stride = soa ? t->soa_stride : t->rec_bytes;
+  p.code_bytes = t->code_bytes;
+  p.stage_bytes = stage_bytes(t, soa, &p.alpha_slot);
+  p.lut = t->lut_dev;
+  p.idx = idx;
+  p.n = n;
+  p.out = out;
+  p.status = t->status_dev;
+
+  int nwarps = cpk::kMaxWarps;
+  auto smem_for = [&](int w) {
+    return static_cast<size_t>(cpk::kLutBytes) + static_cast<size_t>(w) * pf * p.stage_bytes +
+           static_cast<size_t>(w) * pf * 4;
+  };
+  while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
+  const size_t smem = smem_for(nwarps);
+  if (smem > static_cast<size_t>(t->max_smem)) {
+    g_last_error = "geometry needs more shared memory than the device offers";
+    return CP_ERR_INVALID_ARG;
+  }
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  // Persistent grid: one CTA per SM (the LUT takes most of shared memory), or
+  // fewer when there are fewer lookups than warps.
+  uint64_t blocks = (n + nwarps - 1) / nwarps;
+  if (blocks > static_cast<uint64_t>(t->sm_count)) blocks = t->sm_count;
+  void* args[] = {&p};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
+                       dim3(nwarps * 32), args, smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
+  return CP_OK;
+}
+
+cp_status decode_common(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                        void* stream, int want_residency) {
+  if (t == nullptr) return CP_ERR_INVALID_ARG;
+  if (t->residency != want_residency) {
+    g_last_error = want_residency == CP_RESIDENT_DEVICE
+                       ? "table is host-resident: use cp_lookup_decode_host"
+                       : "table is device-resident: use cp_lookup_decode";
+    return CP_ERR_INVALID_ARG;
+  }
+  if (n == 0) return CP_OK;
+  if (n > kMaxLookups || idx == nullptr || out == nullptr || !aligned(idx, 8) ||
+      !aligned(out, 16)) {
+    g_last_error = "bad ids/output pointer, alignment or count";
+    return CP_ERR_INVALID_ARG;
+  }
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != t->device) {
+    g_last_error = "current device differs from the table's device";
+    return CP_ERR_INVALID_ARG;
+  }
+  return launch_decode(t, idx, n, out, static_cast<cudaStream_t>(stream),
+                       want_residency == CP_RESIDENT_HOST);
+}
+
+}  // namespace
+
+namespace cpk {
+
+__global__ void repack_soa_kernel(const uint8_t* __restrict__ rec, uint64_t n_rows, uint32_t R,
+                                  uint32_t code_bytes, uint32_t S, uint8_t* __restrict__ codes,
+                                  uint16_t* __restrict__ alpha) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t r = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < n_rows; r += warps) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(rec + r * R);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(codes + r * S);
+    for (uint32_t i = lane; i < S / 2; i += 32) dst[i] = (2 * i < code_bytes) ? src[i] : 0;
+    if (lane == 0) alpha[r] = src[code_bytes / 2];
+  }
+}
+
+}  // namespace cpk
+
+extern "C" {
+
+uint64_t cp_record_bytes(uint32_t d, uint32_t bits_per_step) {
+  if (!geometry_ok(d, bits_per_step)) return 0;
+  return static_cast<uint64_t>(d) * bits_per_step / 16 + 2;
+}
+
+uint64_t cp_soa_bytes(uint64_t n_rows, uint32_t d, uint32_t bits_per_step) {
+  if (!geometry_ok(d, bits_per_step) || n_rows == 0 || n_rows > kMaxRows) return 0;
+  const uint64_t codes = n_rows * soa_stride(d, bits_per_step);
+  const uint64_t alph = (n_rows * 2 + 15) & ~15ull;
+  return codes + alph;
+}
+
+const char* cp_status_string(cp_status s) {
+  switch (s) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG";
+    case CP_ERR_INDEX_OOB: return "CP_ERR_INDEX_OOB";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA";
+    case CP_ERR_NO_MEMORY: return "CP_ERR_NO_MEMORY";
+    case CP_ERR_FORMAT: return "CP_ERR_FORMAT";
+  }
+  return "CP_ERR_UNKNOWN";
+}
+
+const char* cp_last_error(void) { return g_last_error.c_str(); }
+
+cp_status cp_test_inject_failure(int kind, int count) {
+  if (kind == 1) g_fail_alloc.store(count);
+  else if (kind == 2) g_fail_register.store(count);
+  else return CP_ERR_INVALID_ARG;
+  return CP_OK;
+}
+
+void cp_table_free(cp_table* t) {
+  if (t == nullptr) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != t->device) cudaSetDevice(t->device);
+  if (t->lut_dev) cudaFree(t->lut_dev);
+  if (t->status_dev) cudaFree(t->status_dev);
+  if (t->registered) cudaHostUnregister(t->registered);
+  if (prev >= 0 && prev != t->device) cudaSetDevice(prev);
+  delete t;
+}
+
+cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, uint32_t d,
+                        uint32_t bits_per_step, const uint16_t* lut_fp16, int residency,
+                        int layout, void* soa_dst, void* stream) {
+  if (out == nullptr) return CP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (records == nullptr || lut_fp16 == nullptr || n_rows == 0 || n_rows > kMaxRows ||
+      !geometry_ok(d, bits_per_step) || !aligned(records, 16)) {
+    g_last_error = "bad records pointer/alignment, LUT pointer or geometry";
+    return CP_ERR_INVALID_ARG;
+  }
+  if (residency != CP_RESIDENT_DEVICE && residency != CP_RESIDENT_HOST) return CP_ERR_INVALID_ARG;
+  if (layout != CP_LAYOUT_AOS && layout != CP_LAYOUT_SOA) return CP_ERR_INVALID_ARG;
+  if (layout == CP_LAYOUT_SOA && (soa_dst == nullptr || !aligned(soa_dst, 16))) {
+    g_last_error = "CP_LAYOUT_SOA needs a 16-byte aligned soa_dst";
+    return CP_ERR_INVALID_ARG;
+  }
+  if (layout == CP_LAYOUT_AOS && soa_dst != nullptr) return CP_ERR_INVALID_ARG;
+  for (int i = 0; i < 1024; ++i) {
+    if ((lut_fp16[i] & 0x7c00u) == 0x7c00u) {
+      g_last_error = "LUT holds a non-finite fp16 value";
+      return CP_ERR_FORMAT;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  cp_table* t = new (std::nothrow) cp_table();
+  if (t == nullptr) return CP_ERR_NO_MEMORY;
+  cudaGetDevice(&t->device);
+  t->residency = residency;
+  t->layout = layout;
+  t->n_rows = n_rows;
+  t->d = d;
+  t->k = bits_per_step;
+  t->code_bytes = d * bits_per_step / 16;
+  t->rec_bytes = t->code_bytes + 2;
+  t->soa_stride = soa_stride(d, bits_per_step);
+  t->kernels = kernels_for(bits_per_step);
+  cudaDeviceGetAttribute(&t->sm_count, cudaDevAttrMultiProcessorCount, t->device);
+  cudaDeviceGetAttribute(&t->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, t->device);
+
+  cp_status st = CP_OK;
+  cudaError_t e;
+  if (take_injected(g_fail_alloc)) {
+    g_last_error = "injected device allocation failure";
+    delete t;
+    return CP_ERR_NO_MEMORY;
+  }
+  e = cudaMalloc(&t->lut_dev, 512 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&t->status_dev, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaMalloc");
+    cp_table_free(t);
+    return CP_ERR_NO_MEMORY;
+  }
+  e = cudaMemcpyAsync(t->lut_dev, lut_fp16, 2048, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(t->status_dev, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) {
+    st = cuda_fail(e, "LUT upload");
+    cp_table_free(t);
+    return st;
+  }
+  const uint64_t table_bytes = n_rows * t->rec_bytes;
+  if (residency == CP_RESIDENT_HOST) {
+    void* dptr = nullptr;
+    if (take_injected(g_fail_register)) {
+      g_last_error = "injected host registration failure";
+      cp_table_free(t);
+      return CP_ERR_CUDA;
+    }
+    e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(records), 0);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // not page-locked: register it ourselves
+      e = cudaHostRegister(const_cast<void*>(records), table_bytes,
+                           cudaHostRegisterMapped | cudaHostRegisterReadOnly);
+      if (e != cudaSuccess) {   // read-only registration is optional on some systems
+        cudaGetLastError();
+        e = cudaHostRegister(const_cast<void*>(records), table_bytes, cudaHostRegisterMapped);
+      }
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "cudaHostRegister");
+        cp_table_free(t);
+        return st;
+      }
+      t->registered = const_cast<void*>(records);
+      e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(records), 0);
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "cudaHostGetDevicePointer");
+        cp_table_free(t);
+        return st;
+      }
+    }
+    t->rec = static_cast<const uint8_t*>(dptr);
+    if (!aligned(t->rec, 16)) {
+      g_last_error = "device alias of the host table is not 16-byte aligned";
+      cp_table_free(t);
+      return CP_ERR_INVALID_ARG;
+    }
+  } else {
+    t->rec = static_cast<const uint8_t*>(records);
+  }
+  if (layout == CP_LAYOUT_SOA) {
+    uint8_t* codes = static_cast<uint8_t*>(soa_dst);
+    if (residency == CP_RESIDENT_HOST) {
+      void* dptr = nullptr;
+      e = cudaHostGetDevicePointer(&dptr, soa_dst, 0);
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "cudaHostGetDevicePointer(soa_dst)");
+        cp_table_free(t);
+        return st;
+      }
+      codes = static_cast<uint8_t*>(dptr);
+    }
+    t->soa_codes = codes;
+    t->soa_alpha = reinterpret_cast<const uint16_t*>(codes + n_rows * t->soa_stride);
+    const uint64_t warps = n_rows < (1ull << 22) ? n_rows : (1ull << 22);
+    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+    cpk::repack_soa_kernel<<<blocks, 256, 0, s>>>(t->rec, n_rows, t->rec_bytes, t->code_bytes,
+                                                  t->soa_stride, codes,
+                                                  const_cast<uint16_t*>(t->soa_alpha));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "SoA repack launch");
+      cp_table_free(t);
+      return st;
+    }
+  }
+  *out = t;
+  return CP_OK;
+}
+
+cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                           void* stream) {
+  return decode_common(t, idx, n, out, stream, CP_RESIDENT_DEVICE);
+}
+
+cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t n,
+                                uint16_t* out, void* stream) {
+  return decode_common(t, idx, n, out, stream, CP_RESIDENT_HOST);
+}
+
+cp_status cp_get_status(const cp_table* t, void* stream) {
+  if (t == nullptr) return CP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t h = 0;
+  e = cudaMemcpyAsync(&h, t->status_dev, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(t->status_dev, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status readback");
+  return (h & 1u) ? CP_ERR_INDEX_OOB : CP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,16 @@
+// Instantiations of the lookup-decode kernel for k = 4 bits per trellis step.
+#include "cp_kernels.cuh"
+#include "cp_dispatch.h"
+
+namespace cpk {
+
+KernelSet kernels_k4() {
+  KernelSet s;
+  s.aos_dev = &lookup_decode_kernel<4, false, kPfDevice>;
+  s.soa_dev = &lookup_decode_kernel<4, true, kPfDevice>;
+  s.aos_host = &lookup_decode_kernel<4, false, kPfHost>;
+  s.soa_host = &lookup_decode_kernel<4, true, kPfHost>;
+  return s;
+}
+
+}  // namespace cpk

@@ -239,12 +239,14 @@ def time_steps(fn, steps, warmup, flush, stream):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
+    torch.cuda.nvtx.range_push("timed")
     for a, b in ev:
         a.record(stream)
         fn()
         b.record(stream)
         flush.zero_()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
 
 

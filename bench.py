@@ -4,8 +4,9 @@ A step is one cp_lookup_decode over the whole replay batch (default: the
 DeepSeek-scale table, 1.98e8 rows x d=1024 at b=2 = 51 GB of records in HBM,
 4096 tokens x 48 rows = 196,608 Zipf(1.0) lookups).  W untimed warm-up steps,
 then K timed steps; each step is bracketed by CUDA events on the launching
-stream and followed (outside the timed interval) by a 512 MB write that flushes
-the 129 MB L2, so no step reuses the previous step's records from L2.
+stream and followed (outside the timed interval) by a 512 MB write and a 512 MB
+read that flush the 129 MB L2, so no step reuses the previous step's records
+from L2 and no dirty flush lines are written back inside the next step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--layout aos|soa] [--host-path]
@@ -38,7 +39,7 @@ sys.path.insert(0, str(ROOT))
 
 FALLBACK_HBM_GBS = 6800.0       # earlier GB300 copy measurement, used when no measured file
 PAGES_LATENCY_S = 0.190e-3      # pages' HBM-resident replay latency on one H200
-L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_BYTES = 1024 << 20     # 512 MB written + 512 MB read between steps
 METRIC = "CP lookup-decode rows/s & achieved HBM GB/s, 4096-tok×48-row replay"
 
 
@@ -230,12 +231,25 @@ def build_table(w, layout: str, seed: int):
     return table, rec, soa
 
 
+def flush_l2(flush):
+    """Write the first half of `flush` (> L2), then read the second half so the
+    written lines leave L2 before the next timed step (outside the timed interval)."""
+    half = flush.numel() // 2
+    flush[:half].zero_()
+    flush[half:].view(torch_int64()).amax()
+
+
+def torch_int64():
+    import torch
+    return torch.int64
+
+
 def time_steps(fn, steps, warmup, flush, stream):
     """Per-step device times (s) of fn() with an L2 flush between steps."""
     import torch
     for _ in range(warmup):
         fn()
-        flush.zero_()
+        flush_l2(flush)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -244,7 +258,7 @@ def time_steps(fn, steps, warmup, flush, stream):
         a.record(stream)
         fn()
         b.record(stream)
-        flush.zero_()
+        flush_l2(flush)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
@@ -329,7 +343,7 @@ def our_arm(args, w, rank, world, local):
                        "rows_per_token": w.rows_per_token,
                        "index_dist": f"{w.dist}({w.zipf_s})", "layout": args.layout,
                        "table_gb": w.table_bytes / 1e9,
-                       "l2": "flushed between steps (512 MB write, outside the timed interval)",
+                       "l2": "flushed between steps (512 MB write then 512 MB read, outside the timed interval)",
                        "parallelism": f"replicas x{world}"},
             "achieved_gbs_algorithmic": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -40,7 +40,8 @@
  *     queued; nothing is written in that case.
  *   - The caller owns every large buffer (records, SoA copy, ids, output); a
  *     table handle borrows them and they must outlive it.  The handle owns only
- *     its LUT copy, its device status word and its geometry.
+ *     its LUT copy, its device status word, its geometry and, for host-resident
+ *     tables, 32 MB of device scratch for deduplication and the visiting order.
  *   - Out-of-range ids never fault: the output row is written as zeros and the
  *     table's device status word records CP_ERR_INDEX_OOB for cp_get_status.
  *   - n = 0 is a valid no-op.
@@ -127,7 +128,16 @@ cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, ui
  * cp_lookup_decode_host -- the same operation for a CP_RESIDENT_HOST table: the
  * kernel reads only the requested records directly from pinned host DRAM over
  * the host link (zero-copy) [P4 "assumptions and limits"; P1 "Interpretation"].
- * idx and out are device pointers as for cp_lookup_decode.
+ * idx and out are device pointers as for cp_lookup_decode; the output is the
+ * same, bit for bit, as cp_lookup_decode on the same records.
+ * Internally, per pass of at most 2^20 lookups: one lookup per distinct id is
+ * elected owner (a device hash table), only owners' records cross the host link,
+ * visited grouped by row-id range (a counting partition into 4096 ranges) so
+ * that successive host reads are close in the host address space; every other
+ * lookup then copies its owner's finished row.  This state lives in 32 MB of
+ * device scratch owned by the handle (allocated by cp_table_load), so calls on
+ * one host-resident handle must be ordered on one stream (or otherwise
+ * serialised).
  */
 cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t n,
                                 uint16_t* out, void* stream);

@@ -223,12 +223,29 @@ def test_host_resident_parity(lut, pinned, layout):
     table = cp.load_table(host, n_rows, d, k, lut, layout=layout, soa=soa)
     idx = synth.zipf_indices(9, n, n_rows)
     idx[-1] = n_rows - 1
+    idx[5:9] = [-1, n_rows, 1 << 45, -(1 << 40)]          # out of range: zero rows
     got = _run(table, idx, layout_host=True).reshape(n, d)
-    assert cp.get_status(table) == cp.CP_OK
+    assert cp.get_status(table) == cp.CP_ERR_INDEX_OOB
+    assert not got[5:9].any()
     dev_table = cp.load_table(rec_cpu.cuda(), n_rows, d, k, lut)
     assert np.array_equal(got, _run(dev_table, idx).reshape(n, d))
     _assert_exact(got, oracle_decode(SEED, d, k, idx, n_rows, lut), "host-resident")
     table.close()
+
+
+def test_host_resident_multi_pass(lut):
+    """More lookups than one pass (2^20), most of them repeated ids: passes chain on the stream."""
+    d, k, n_rows = 8, 4, 100003
+    n = (1 << 20) * 2 + 12345
+    rec_cpu = synth.gen_records(SEED, torch.arange(n_rows), d, k).reshape(-1).contiguous()
+    table = cp.load_table(rec_cpu.pin_memory(), n_rows, d, k, lut)
+    idx = synth.uniform_indices(4, n, n_rows)
+    got = _run(table, idx, layout_host=True).reshape(n, d)
+    dev = cp.load_table(rec_cpu.cuda(), n_rows, d, k, lut)
+    assert np.array_equal(got, _run(dev, idx).reshape(n, d))
+    rng = np.random.default_rng(3)
+    js = np.unique(np.concatenate([rng.integers(0, n, 4000), [0, n - 1, (1 << 20) - 1, 1 << 20]]))
+    _assert_exact(got[js], oracle_decode(SEED, d, k, idx[js], n_rows, lut), "multi-pass")
 
 
 # ---------------------------------------------------------------------------

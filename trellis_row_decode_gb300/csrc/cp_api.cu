@@ -27,6 +27,11 @@ struct cp_table {
   const uint16_t* soa_alpha;
   uint32_t* lut_dev;      // 512 words
   uint32_t* status_dev;   // 1 word
+  void* scratch_dev;      // host-resident tables: dedupe keys (kHashSlotsMax x 8 B),
+                          // owners (kHashSlotsMax), dup (kBucketChunk), bucket counts
+                          // (nb + 1, padded), visiting order (kBucketChunk)
+  uint32_t bucket_shift;  // bucket of row r = r >> bucket_shift
+  uint32_t bucket_nb;     // number of row-range buckets
   void* registered;       // host range this handle registered, else nullptr
   int sm_count;
   int max_smem;           // opt-in shared memory per block
@@ -76,25 +81,27 @@ cpk::KernelSet kernels_for(uint32_t k) {
   }
 }
 
-// Stage size in bytes for a geometry: the 16-byte aligned span that holds the
-// record (misalignment <= 14 bytes for AoS), plus 16 bytes of slack for the
-// 64-bit funnel reads past the code; SoA adds the 4-byte alpha slot.
+// Stage size in bytes for a geometry: a 16-byte prefix (room for the spliced
+// code tail below bit 0), the 16-byte aligned span that holds the record
+// (misalignment <= 14 bytes for AoS), and 16 bytes of slack for the 64-bit
+// funnel reads past the code; SoA adds the 4-byte alpha slot in that slack.
 uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot) {
+  const uint32_t pre = cpk::kStagePrefix;
   if (soa) {
-    *alpha_slot = t->soa_stride + 8;
-    return t->soa_stride + 16;
+    *alpha_slot = pre + t->soa_stride + 8;
+    return pre + t->soa_stride + 16;
   }
   *alpha_slot = 0;
   const uint32_t span = t->code_bytes + 2 + 14;
-  return ((span + 15u) & ~15u) + 16u;
+  return pre + ((span + 15u) & ~15u) + 16u;
 }
 
 cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                         cudaStream_t stream, bool host_path) {
   const bool soa = (t->layout == CP_LAYOUT_SOA);
   const int pf = host_path ? cpk::kPfHost : cpk::kPfDevice;
-  cpk::DecodeFn fn = host_path ? (soa ? t->kernels.soa_host : t->kernels.aos_host)
-                               : (soa ? t->kernels.soa_dev : t->kernels.aos_dev);
+  const int ci = cpk::cpl_index(t->d);
+  cpk::DecodeFn fn = host_path ? t->kernels.host[soa ? 1 : 0][ci] : t->kernels.dev[soa ? 1 : 0][ci];
   cpk::DecodeParams p;
   std::memset(&p, 0, sizeof(p));
   p.codes = soa ? t->soa_codes : t->rec;
@@ -114,7 +121,7 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   int nwarps = cpk::kMaxWarps;
   auto smem_for = [&](int w) {
     return static_cast<size_t>(cpk::kLutBytes) + static_cast<size_t>(w) * pf * p.stage_bytes +
-           static_cast<size_t>(w) * pf * 4;
+           static_cast<size_t>(w) * pf * 8;
   };
   while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
   const size_t smem = smem_for(nwarps);
@@ -130,10 +137,54 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   // fewer when there are fewer lookups than warps.
   uint64_t blocks = (n + nwarps - 1) / nwarps;
   if (blocks > static_cast<uint64_t>(t->sm_count)) blocks = t->sm_count;
-  void* args[] = {&p};
-  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
-                       dim3(nwarps * 32), args, smem, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
+  if (n / (blocks * nwarps) >= (1ull << 31)) {   // rows per warp are counted in 32 bits
+    g_last_error = "too many lookups for one launch";
+    return CP_ERR_INVALID_ARG;
+  }
+  if (!host_path) {
+    void* args[] = {&p};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
+                         dim3(nwarps * 32), args, smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
+    return CP_OK;
+  }
+  // Host-resident table, per pass of at most kBucketChunk lookups: elect one
+  // owner per distinct id, partition the owners by row range, decode them in
+  // that order (each row lands at its own position), then fill the other
+  // lookups from their owner's row.
+  unsigned long long* keys = static_cast<unsigned long long*>(t->scratch_dev);
+  uint32_t* owner = reinterpret_cast<uint32_t*>(keys + cpk::kHashSlotsMax);
+  uint32_t* dup = owner + cpk::kHashSlotsMax;
+  uint32_t* counts = dup + cpk::kBucketChunk;
+  uint32_t* perm = counts + ((t->bucket_nb + 1 + 63) & ~63u);
+  for (uint64_t c0 = 0; c0 < n; c0 += cpk::kBucketChunk) {
+    const uint64_t m = (n - c0 < cpk::kBucketChunk) ? n - c0 : cpk::kBucketChunk;
+    uint32_t ts = 1024;
+    while (ts < 2 * m) ts <<= 1;
+    e = cudaMemsetAsync(keys, 0, ts * sizeof(unsigned long long), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(owner, 0xFF, ts * sizeof(uint32_t), stream);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(counts, 0, (t->bucket_nb + 1) * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch reset");
+    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, t->sm_count, stream);
+    cpk::launch_bucket_partition(idx + c0, dup, m, t->n_rows, t->bucket_shift, t->bucket_nb,
+                                 counts, perm, t->sm_count, stream);
+    cpk::DecodeParams pc = p;
+    pc.idx = idx + c0;
+    pc.perm = perm;
+    pc.n_dev = counts + t->bucket_nb;                   // visits = owners + out-of-range ids
+    pc.n = m;
+    pc.out = out + c0 * t->d;
+    uint64_t bl = (m + nwarps - 1) / nwarps;
+    if (bl > static_cast<uint64_t>(t->sm_count)) bl = t->sm_count;
+    void* args[] = {&pc};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(bl)),
+                         dim3(nwarps * 32), args, smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "host lookup-decode launch");
+    cpk::launch_copy_dups(dup, m, t->d, out + c0 * t->d, t->sm_count, stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "host path launch");
+  }
   return CP_OK;
 }
 
@@ -224,6 +275,7 @@ void cp_table_free(cp_table* t) {
   if (prev != t->device) cudaSetDevice(t->device);
   if (t->lut_dev) cudaFree(t->lut_dev);
   if (t->status_dev) cudaFree(t->status_dev);
+  if (t->scratch_dev) cudaFree(t->scratch_dev);
   if (t->registered) cudaHostUnregister(t->registered);
   if (prev >= 0 && prev != t->device) cudaSetDevice(prev);
   delete t;
@@ -292,6 +344,25 @@ cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, ui
   }
   const uint64_t table_bytes = n_rows * t->rec_bytes;
   if (residency == CP_RESIDENT_HOST) {
+    // row-range buckets of the visiting order: at most 2^kBucketBits of them
+    uint32_t bits = 0;
+    while (bits < 64 && ((n_rows - 1) >> bits) != 0) ++bits;
+    t->bucket_shift = bits > cpk::kBucketBits ? bits - cpk::kBucketBits : 0;
+    t->bucket_nb = static_cast<uint32_t>(((n_rows - 1) >> t->bucket_shift) + 1);
+    const size_t bytes = cpk::kHashSlotsMax * (sizeof(unsigned long long) + sizeof(uint32_t)) +
+                         (static_cast<size_t>(cpk::kBucketChunk) * 2 +
+                          ((t->bucket_nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
+    if (take_injected(g_fail_alloc)) {
+      g_last_error = "injected device allocation failure";
+      cp_table_free(t);
+      return CP_ERR_NO_MEMORY;
+    }
+    e = cudaMalloc(&t->scratch_dev, bytes);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaMalloc(bucket scratch)");
+      cp_table_free(t);
+      return CP_ERR_NO_MEMORY;
+    }
     void* dptr = nullptr;
     if (take_injected(g_fail_register)) {
       g_last_error = "injected host registration failure";

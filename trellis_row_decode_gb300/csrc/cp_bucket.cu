@@ -1,0 +1,183 @@
+// cp_bucket.cu -- processing order for host-resident tables.
+//
+// The pages place the table either in HBM or in pinned host DRAM read over the
+// host link ("2비트 코드와 공유 트렐리스로 n-gram 룩업 테이블을 4~8배 압축한다",
+// section 전제와 한계).  Over the host link the cost of a random record read
+// depends on how far apart successive reads are in the host address space
+// (address translation), so the host path visits the lookups grouped by row-id
+// range: a counting partition into 2^12 ranges.  Only the visiting order
+// changes; every output row is still written at its own lookup position.
+//
+// Repeated ids are fetched once (the pages name frequency-based caching as a
+// lever for the host placement; with Zipf-distributed lookups about half of the
+// ids of a replay repeat): a device hash table elects one owner lookup per
+// distinct id, only owners are partitioned and decoded, and the other lookups
+// copy their owner's finished output row.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "cp_dispatch.h"
+
+namespace cpk {
+
+namespace {
+
+constexpr uint32_t kNoOwner = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t bucket_of(int64_t r, uint64_t n_rows, uint32_t shift,
+                                              uint32_t nb) {
+  return (static_cast<uint64_t>(r) < n_rows) ? static_cast<uint32_t>(static_cast<uint64_t>(r) >> shift)
+                                             : nb;
+}
+
+// Lookup j takes part in the partition when it owns its id, or its id is out
+// of range (it then writes a zero row).  dup == nullptr: every lookup does.
+__device__ __forceinline__ bool visits(const uint32_t* dup, uint64_t j) {
+  if (dup == nullptr) return true;
+  const uint32_t o = dup[j];
+  return o == static_cast<uint32_t>(j) || o == kNoOwner;
+}
+
+// dup[j] = the owner lookup of idx[j] (the first to claim the id's slot in an
+// open-addressing table of ts = 2^k slots, keys r + 1, 0 = empty), or kNoOwner
+// for an id outside [0, n_rows).  Probing is bounded by ts; a lookup that
+// finds no slot owns itself (still correct, just not deduplicated).
+__global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint64_t n_rows,
+                              unsigned long long* __restrict__ keys, uint32_t* __restrict__ owner,
+                              uint32_t ts, uint32_t* __restrict__ dup) {
+  const uint64_t T = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n; j += T) {
+    const int64_t r = __ldg(idx + j);
+    if (static_cast<uint64_t>(r) >= n_rows) {
+      dup[j] = kNoOwner;
+      continue;
+    }
+    const unsigned long long key = static_cast<unsigned long long>(r) + 1ull;
+    uint32_t slot = static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
+    uint32_t o = static_cast<uint32_t>(j);
+    for (uint32_t probe = 0; probe < ts; ++probe) {
+      const unsigned long long prev = atomicCAS(keys + slot, 0ull, key);
+      if (prev == 0ull || prev == key) {
+        const uint32_t w = atomicCAS(owner + slot, kNoOwner, static_cast<uint32_t>(j));
+        o = (w == kNoOwner) ? static_cast<uint32_t>(j) : w;
+        break;
+      }
+      slot = (slot + 1) & (ts - 1);
+    }
+    dup[j] = o;
+  }
+}
+
+// Non-owner lookups copy their owner's decoded row (warp per row).
+__global__ void copy_dups_kernel(const uint32_t* __restrict__ dup, uint64_t n, uint32_t row16,
+                                 uint4* __restrict__ out) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       j < n; j += warps) {
+    const uint32_t o = dup[j];
+    if (o == kNoOwner || o == static_cast<uint32_t>(j)) continue;
+    const uint4* src = out + static_cast<uint64_t>(o) * row16;
+    uint4* dst = out + j * row16;
+    for (uint32_t c = lane; c < row16; c += 32) __stcs(dst + c, __ldcg(src + c));
+  }
+}
+
+// counts[b] += number of lookups in bucket b (shared-memory histogram per CTA).
+__global__ void bucket_count_kernel(const int64_t* __restrict__ idx, const uint32_t* __restrict__ dup,
+                                    uint64_t n, uint64_t n_rows, uint32_t shift, uint32_t nb,
+                                    uint32_t* __restrict__ counts) {
+  extern __shared__ uint32_t hist[];                    // nb + 1 bins
+  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const uint64_t lo = blockIdx.x * n / gridDim.x, hi = (blockIdx.x + 1) * n / gridDim.x;
+  for (uint64_t j = lo + threadIdx.x; j < hi; j += blockDim.x)
+    if (visits(dup, j)) atomicAdd(&hist[bucket_of(__ldg(idx + j), n_rows, shift, nb)], 1u);
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x)
+    if (hist[i]) atomicAdd(&counts[i], hist[i]);
+}
+
+// In-place exclusive prefix sum of len words, one CTA of 1024 threads.
+__global__ void bucket_scan_kernel(uint32_t* __restrict__ counts, uint32_t len) {
+  __shared__ uint32_t warp_sum[32];
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t per = (len + blockDim.x - 1) / blockDim.x;
+  const uint32_t b0 = tid * per;
+  const uint32_t b1 = (b0 + per < len) ? b0 + per : len;
+  uint32_t s = 0;
+  for (uint32_t i = b0; i < b1; ++i) s += counts[i];
+  uint32_t inc = s;                                     // inclusive scan inside the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= static_cast<uint32_t>(o)) inc += v;
+  }
+  if (lane == 31) warp_sum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t nwarps = blockDim.x >> 5;
+    uint32_t w = (lane < nwarps) ? warp_sum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= static_cast<uint32_t>(o)) w += v;
+    }
+    if (lane < nwarps) warp_sum[lane] = w;             // inclusive over warps
+  }
+  __syncthreads();
+  uint32_t run = inc - s + (warp > 0 ? warp_sum[warp - 1] : 0);
+  for (uint32_t i = b0; i < b1; ++i) {
+    const uint32_t v = counts[i];
+    counts[i] = run;
+    run += v;
+  }
+}
+
+// perm[cursor[b]++] = j, one atomic per (warp, bucket) group.
+__global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, const uint32_t* __restrict__ dup,
+                                      uint64_t n, uint64_t n_rows, uint32_t shift, uint32_t nb,
+                                      uint32_t* __restrict__ cursor, uint32_t* __restrict__ perm) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
+       base < n; base += warps * 32) {
+    const uint64_t j = base + lane;
+    const bool valid = j < n && visits(dup, j);
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+      const uint32_t b = bucket_of(__ldg(idx + j), n_rows, shift, nb);
+      const uint32_t group = __match_any_sync(active, b);
+      const uint32_t leader = __ffs(group) - 1;
+      const uint32_t rank = __popc(group & ((1u << lane) - 1u));
+      uint32_t start = 0;
+      if (lane == leader) start = atomicAdd(&cursor[b], static_cast<uint32_t>(__popc(group)));
+      start = __shfl_sync(group, start, leader);
+      perm[start + rank] = static_cast<uint32_t>(j);
+    }
+  }
+}
+
+}  // namespace
+
+void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
+                   uint32_t* owner, uint32_t ts, uint32_t* dup, int sm_count, cudaStream_t s) {
+  dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(idx, n, n_rows, keys, owner, ts,
+                                                                     dup);
+}
+
+void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,
+                             uint32_t shift, uint32_t nb, uint32_t* counts, uint32_t* perm,
+                             int sm_count, cudaStream_t s) {
+  const unsigned blocks = static_cast<unsigned>(sm_count);
+  bucket_count_kernel<<<blocks, 512, (nb + 1) * sizeof(uint32_t), s>>>(idx, dup, n, n_rows, shift,
+                                                                       nb, counts);
+  bucket_scan_kernel<<<1, 1024, 0, s>>>(counts, nb + 1);
+  bucket_scatter_kernel<<<blocks, 512, 0, s>>>(idx, dup, n, n_rows, shift, nb, counts, perm);
+}
+
+void launch_copy_dups(const uint32_t* dup, uint64_t n, uint32_t d, uint16_t* out, int sm_count,
+                      cudaStream_t s) {
+  copy_dups_kernel<<<static_cast<unsigned>(sm_count) * 2, 1024, 0, s>>>(
+      dup, n, d / 8, reinterpret_cast<uint4*>(out));
+}
+
+}  // namespace cpk

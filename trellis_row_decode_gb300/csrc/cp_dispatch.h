@@ -7,17 +7,55 @@ namespace cpk {
 
 // Stages of the per-warp record ring: one row ahead for HBM-resident tables,
 // more rows in flight for tables read over the host link (higher latency).
-constexpr int kPfDevice = 2;
-constexpr int kPfHost = 8;
+#ifndef CP_PF_DEVICE
+#define CP_PF_DEVICE 2
+#endif
+#ifndef CP_PF_HOST
+#define CP_PF_HOST 8
+#endif
+constexpr int kPfDevice = CP_PF_DEVICE;
+constexpr int kPfHost = CP_PF_HOST;
 
 using DecodeFn = void (*)(DecodeParams);
 
+// Chunks-per-lane specialisations: index 0 = any d (runtime loop), index i > 0
+// = d == 256 * kCplValues[i].
+constexpr int kCplVariants = 6;
+constexpr int kCplValues[kCplVariants] = {0, 1, 2, 4, 8, 16};
+
+inline int cpl_index(uint32_t d) {
+  for (int i = 1; i < kCplVariants; ++i)
+    if (d == 256u * static_cast<uint32_t>(kCplValues[i])) return i;
+  return 0;
+}
+
 struct KernelSet {
-  DecodeFn aos_dev;
-  DecodeFn soa_dev;
-  DecodeFn aos_host;
-  DecodeFn soa_host;
+  DecodeFn dev[2][kCplVariants];    // [layout AoS/SoA][cpl index], lookup order
+  DecodeFn host[2][kCplVariants];   // bucketed order (PERM)
 };
+
+// Host-resident tables: lookups are visited bucketed by row-id range so that
+// consecutive records of a warp are close in the host address space.
+constexpr uint32_t kBucketBits = 12;                  // 4096 ranges
+constexpr uint32_t kBucketChunk = 1u << 20;           // lookups per pass
+constexpr uint32_t kHashSlotsMax = 2 * kBucketChunk;  // dedupe table slots (load <= 1/2)
+
+// dup[j] = owner lookup of idx[j] among n lookups (kNoOwner for ids outside
+// [0, n_rows)); keys (ts 64-bit words, zeroed) and owner (ts words, 0xFF-filled)
+// are the open-addressing table, ts a power of two >= 2n.
+void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
+                   uint32_t* owner, uint32_t ts, uint32_t* dup, int sm_count, cudaStream_t s);
+
+// Partition of the lookups that own their id (all of them if dup is null) by
+// (id >> shift), ids outside [0, n_rows) in the last bucket.  counts: nb + 1
+// words, zeroed by the caller; afterwards counts[nb] = number of visits.
+void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,
+                             uint32_t shift, uint32_t nb, uint32_t* counts, uint32_t* perm,
+                             int sm_count, cudaStream_t s);
+
+// out row j = out row dup[j] for every non-owner lookup j.
+void launch_copy_dups(const uint32_t* dup, uint64_t n, uint32_t d, uint16_t* out, int sm_count,
+                      cudaStream_t s);
 
 KernelSet kernels_k3();
 KernelSet kernels_k4();

@@ -17,13 +17,23 @@
 //     entries (the sign of y1 folded in, indexed by hash bits 14..23) and
 //     replicated 32 times, word (entry * 32 + lane): every lane reads its own
 //     bank, so a warp-wide LUT read is one wavefront;
+//   * a record lands 16 bytes into its stage; once it has arrived, lane 0 copies
+//     the code's last 16 bits (a whole halfword, since d*k/16 is even) to the
+//     two bytes just below code bit 0, so the tail-biting wrap (windows that
+//     start below bit 0 take the code's last bits) becomes a plain linear read;
 //   * a lane produces 8 outputs (4 trellis steps, 16 bytes) per chunk; chunk c
 //     needs code bits [k(4c+1) - 16, k(4c+4)), at most 34 bits, read from the
-//     stage as one 64-bit funnel of two words; chunks with negative start
-//     (tail-biting wrap) splice the code's last bits below its first bits;
-//   * per step: hash (one IMAD), index (shift + and), one LDS, fp16 -> fp32,
-//     two fp32 products by alpha (exact: 8 x 11 significant bits), one
-//     cvt.rn.bf16x2; each chunk is one 16-byte streaming store (st.global.cs).
+//     stage as one 64-bit funnel of two words; when d = 256 * CPL every lane
+//     owns exactly CPL chunks c = lane + 32m whose bit offsets differ by 128k
+//     (4k whole words), so one shift amount serves all of them and every other
+//     offset is an immediate;
+//   * per step: window (shift + and), hash (one IMAD), LUT byte offset (shift +
+//     and, lane OR-ed in), one LDS, then alpha * y for both coordinates as one
+//     mixed-precision fma.rn.f32.f16 each (alpha as fp16: exact for |alpha| in
+//     [2^-14, 65504] or 0; the fp32 result of fp16 x fp16 is exact) and one
+//     cvt.rn.bf16x2.f32; rows whose alpha is outside that range take an fp32
+//     multiply path with identical results; each chunk is one 16-byte streaming
+//     store (st.global.cs).
 #pragma once
 
 #include <cstdint>
@@ -36,7 +46,10 @@ namespace cpk {
 constexpr int kLutEntries = 1024;                  // 512 pairs x sign of y1
 constexpr int kLutReplicas = 32;                   // one per lane / bank
 constexpr int kLutBytes = kLutEntries * kLutReplicas * 4;   // 128 KB
-constexpr int kMaxWarps = 32;
+#ifndef CP_MAX_WARPS
+#define CP_MAX_WARPS 32
+#endif
+constexpr int kMaxWarps = CP_MAX_WARPS;             // warps per CTA (one CTA per SM)
 
 struct DecodeParams {
   const uint8_t* codes;     // AoS: records base; SoA: code array base (16-byte aligned)
@@ -50,6 +63,8 @@ struct DecodeParams {
   uint32_t alpha_slot;      // SoA: offset of the 4-byte alpha copy inside a stage
   const uint32_t* lut;      // 512 words: fp16 y0 (low half) | fp16 y1 (high half)
   const int64_t* idx;
+  const uint32_t* perm;     // processing order (PERM kernels): position i decodes lookup perm[i]
+  const uint32_t* n_dev;    // PERM kernels: number of positions, read on the device
   uint64_t n;
   uint16_t* out;            // bf16 [n][d], 16-byte aligned
   uint32_t* status;         // bit 0: an id was out of range
@@ -60,16 +75,15 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 
 // 16-byte async copy global -> shared, L2 only; bytes in [1, 16], rest zero-filled.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)),
-               "l"(src), "r"(bytes)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(bytes)
                : "memory");
 }
 
 // 4-byte async copy global -> shared; bytes in [0, 4], rest zero-filled.
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(bytes)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
 }
 
@@ -82,44 +96,90 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+// Exact alpha * (y0, y1) for fp16 alpha: two mixed-precision FMAs with c = -0
+// (x + (-0) = x for every x, signed zeros included).
+__device__ __forceinline__ uint32_t scale_pair_f16(uint32_t v, uint16_t a_h) {
+  float o0, o1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.f16 %0, lo, %3, %4;\n\tfma.rn.f32.f16 %1, hi, %3, %4;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "r"(v), "h"(a_h), "f"(-0.0f));
+  const __nv_bfloat162 r = __floats2bfloat162_rn(o0, o1);
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// 64 bits of the staged bytes starting at bit P (bit 0 = LSB of byte 0).
-// At least 64 - (P & 31) >= 33 of them are meaningful.
-__device__ __forceinline__ uint64_t bits64(const uint32_t* w, uint32_t P) {
-  const uint32_t i = P >> 5;
-  const uint64_t v = (static_cast<uint64_t>(w[i + 1]) << 32) | w[i];
-  return v >> (P & 31);
+// Same result for any bf16 alpha (as fp32): convert, multiply, round.
+__device__ __forceinline__ uint32_t scale_pair_f32(uint32_t v, float a) {
+  const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&v));
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a * y.x, a * y.y);
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Steps 4c..4c+3 of a row: 8 bf16 outputs (16 bytes).
-template <int K>
-__device__ __forceinline__ uint4 decode_chunk(uint64_t x, const uint32_t* lut_lane, float a) {
+// LUT word of state s for this lane: byte offset ((h >> 14) & 1023) * 128 + lane * 4.
+__device__ __forceinline__ uint32_t lut_word(const uint8_t* lut_bytes, uint32_t s, uint32_t lane4) {
+  const uint32_t h = s * s + s;                                   // mod 2^32
+  const uint32_t off = ((h >> 7) & ((kLutEntries - 1) << 7)) | lane4;
+  return *reinterpret_cast<const uint32_t*>(lut_bytes + off);
+}
+
+// Steps 4c..4c+3 of a row from x (bit 0 = first bit of the first window).
+template <int K, bool F16>
+__device__ __forceinline__ uint4 decode_chunk(uint64_t x, const uint8_t* lut_bytes,
+                                              uint32_t lane4, uint16_t a_h, float a) {
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t s = static_cast<uint32_t>(x >> (K * j)) & 0xFFFFu;
-    const uint32_t h = s * s + s;                       // mod 2^32
-    const uint32_t e = (h >> 14) & (kLutEntries - 1);   // bit 9 of e = bit 23 of h (sign)
-    const uint32_t v = lut_lane[e * kLutReplicas];
-    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&v));
-    const __nv_bfloat162 r = __floats2bfloat162_rn(a * y.x, a * y.y);
-    o[j] = *reinterpret_cast<const uint32_t*>(&r);
+    const uint32_t v = lut_word(lut_bytes, s, lane4);
+    o[j] = F16 ? scale_pair_f16(v, a_h) : scale_pair_f32(v, a);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+__device__ __forceinline__ uint64_t funnel64(uint32_t lo, uint32_t hi, uint32_t sh) {
+  return ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
+}
+
+// Decode one staged row into orow (16-byte chunks).  w: staged words; boff: bit
+// offset of code bit 0 in the stage (>= 16 bits of spliced tail below it).
+// CPL > 0: d == 256 * CPL.
+template <int K, int CPL, bool F16>
+__device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uint32_t d,
+                                           const uint8_t* lut_bytes, uint32_t lane,
+                                           uint16_t a_h, float a, uint4* orow) {
+  const uint32_t lane4 = lane << 2;
+  if constexpr (CPL > 0) {
+    // chunk c = lane + 32 m starts at bit boff + K(4 lane + 1) - 16 + 128 K m
+    const uint32_t P0 = boff + K * (4 * lane + 1) - 16;
+    const uint32_t* w0 = w + (P0 >> 5);
+    const uint32_t sh = P0 & 31;
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) {
+      const uint64_t x = funnel64(w0[4 * K * m], w0[4 * K * m + 1], sh);
+      __stcs(orow + lane + 32 * m, decode_chunk<K, F16>(x, lut_bytes, lane4, a_h, a));
+    }
+  } else {
+    const uint32_t C = d >> 3;
+    for (uint32_t c = lane; c < C; c += 32) {
+      const uint32_t P = boff + K * (4 * c + 1) - 16;
+      const uint64_t x = funnel64(w[P >> 5], w[(P >> 5) + 1], P & 31);
+      __stcs(orow + c, decode_chunk<K, F16>(x, lut_bytes, lane4, a_h, a));
+    }
+  }
+}
+
+// Byte offset of the record data inside a stage (room for the spliced tail).
+constexpr uint32_t kStagePrefix = 16;
+
 // K: bits per step (3..6).  SOA: read the SoA copy.  PF: stages per warp.
-template <int K, bool SOA, int PF>
+// CPL: chunks per lane when d == 256 * CPL, 0 for any d (runtime loop).
+// PERM: lookups are visited in the order p.perm (rows still land at their own
+// output position); used to give host-resident tables address locality.
+template <int K, bool SOA, int PF, int CPL, bool PERM>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* lut_s = reinterpret_cast<uint32_t*>(smem);
+  extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
+  const uint32_t lane = tid & 31;
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
 
@@ -128,109 +188,153 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
     const int e = q >> 3;                               // 8 uint4 per entry
     uint32_t v = __ldg(p.lut + (e & 511));
     if (e & 512) v ^= 0x80000000u;
-    reinterpret_cast<uint4*>(lut_s)[q] = make_uint4(v, v, v, v);
+    reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
   }
   __syncthreads();
 
-  uint8_t* stages = smem + kLutBytes + static_cast<size_t>(warp) * PF * p.stage_bytes;
-  uint32_t* meta =
-      reinterpret_cast<uint32_t*>(smem + kLutBytes + static_cast<size_t>(nwarps) * PF * p.stage_bytes) +
-      warp * PF;
-  const uint32_t* lut_lane = lut_s + lane;
+  // Parameters held in registers for the whole loop.
+  const uint32_t stage_bytes = p.stage_bytes;
+  const uint32_t code_bytes = p.code_bytes;
+  const uint32_t d = p.d;
+  const uint64_t n_rows = p.n_rows;
+  const uint64_t stride = p.stride;
+  const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
+  const uintptr_t tbl_end = codes + p.table_bytes;
+  // Records up to 496 bytes (d <= 1024 here) fit one 16-byte copy per lane.
+  constexpr bool kOnePass = (CPL >= 1 && CPL <= 4);
+
+  uint8_t* stages = smem + kLutBytes + static_cast<size_t>(warp) * PF * stage_bytes;
+  // per stage: [0] flags | misalignment << 8, [1] output row (PERM)
+  uint32_t* meta = reinterpret_cast<uint32_t*>(smem + kLutBytes +
+                                               static_cast<size_t>(nwarps) * PF * stage_bytes) +
+                   warp * PF * 2;
+  const uint32_t stages_sa = smem_addr(stages) + kStagePrefix;
 
   const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
-  const uint64_t lo = gw * p.n / W;
-  const uint64_t hi = (gw + 1) * p.n / W;
+  uint64_t n_work = p.n;
+  if (PERM && p.n_dev != nullptr) {
+    const uint64_t nd = *p.n_dev;                        // <= p.n by construction
+    n_work = nd < p.n ? nd : p.n;
+  }
+  const uint64_t lo = gw * n_work / W;
+  const uint64_t hi = (gw + 1) * n_work / W;
   if (lo >= hi) return;
-  const uint64_t cnt = hi - lo;
+  const uint32_t cnt = static_cast<uint32_t>(hi - lo);   // < 2^31 rows per warp (host check)
 
-  // Row ids, 32 per coalesced load, one batch of look-ahead.
+  // Row ids, 32 per coalesced load, one batch of look-ahead.  With PERM the
+  // batch holds positions j = perm[lo + q] and their ids idx[j].
   const int64_t* ids = p.idx + lo;
-  int64_t ib_cur = (static_cast<uint64_t>(lane) < cnt) ? __ldg(ids + lane) : 0;
-  int64_t ib_nxt = (static_cast<uint64_t>(lane) + 32 < cnt) ? __ldg(ids + 32 + lane) : 0;
-  uint64_t batch = 0;
+  const uint32_t* pos = PERM ? p.perm + lo : nullptr;
+  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r) {
+    j = 0;
+    r = 0;
+    if (q < cnt) {
+      if (PERM) {
+        j = __ldg(pos + q);
+        r = __ldg(p.idx + j);
+      } else {
+        r = __ldg(ids + q);
+      }
+    }
+  };
+  uint32_t jb_cur, jb_nxt;
+  int64_t ib_cur, ib_nxt;
+  load_batch(lane, jb_cur, ib_cur);
+  load_batch(lane + 32, jb_nxt, ib_nxt);
+  uint32_t batch = 0;
 
-  const uint32_t C = p.d >> 3;                          // 16-byte chunks per row
-  const uint32_t Lc = (p.d >> 1) * K;                   // code bits per row
-
-  auto issue = [&](uint64_t q) {
+  auto issue = [&](uint32_t q) {
     if (q - batch >= 32) {
       batch += 32;
       ib_cur = ib_nxt;
-      ib_nxt = (batch + 32 + lane < cnt) ? __ldg(ids + batch + 32 + lane) : 0;
+      jb_cur = jb_nxt;
+      load_batch(batch + 32 + lane, jb_nxt, ib_nxt);
     }
     const int64_t r = __shfl_sync(0xffffffffu, ib_cur, static_cast<int>(q - batch));
-    const uint32_t st = static_cast<uint32_t>(q % PF);
-    uint8_t* sb = stages + st * p.stage_bytes;
+    uint32_t jrow = 0;
+    if (PERM) jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
+    const uint32_t st = q & (PF - 1);
+    const uint32_t sa = stages_sa + st * stage_bytes;
     uint32_t m = 0;
-    if (r >= 0 && static_cast<uint64_t>(r) < p.n_rows) {
-      const uint8_t* A = p.codes + static_cast<uint64_t>(r) * p.stride;
-      const uintptr_t a = reinterpret_cast<uintptr_t>(A);
+    if (static_cast<uint64_t>(r) < n_rows) {            // also rejects r < 0
+      const uintptr_t a = codes + static_cast<uint64_t>(r) * stride;
       const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
       const uint32_t mis = static_cast<uint32_t>(a - a0);
-      const uint32_t span = mis + p.code_bytes + (SOA ? 0u : 2u);
-      const uint32_t nch = (span + 15) >> 4;
-      const uintptr_t end = reinterpret_cast<uintptr_t>(p.codes) + p.table_bytes;
-      for (uint32_t c = lane; c < nch; c += 32) {
+      const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+      auto copy = [&](uint32_t c) {
         const uintptr_t src = a0 + 16u * c;
         uint32_t bytes = 16;
-        if (!SOA && src + 16 > end) bytes = static_cast<uint32_t>(end - src);
-        cp_async16(sb + 16u * c, reinterpret_cast<const void*>(src), bytes);
+        if (!SOA) {
+          const uintptr_t left = tbl_end - src;           // > 0: src lies inside the table
+          bytes = left < 16 ? static_cast<uint32_t>(left) : 16u;
+        }
+        cp_async16(sa + 16u * c, reinterpret_cast<const void*>(src), bytes);
+      };
+      if constexpr (kOnePass) {
+        if (lane < nch) copy(lane);
+      } else {
+        for (uint32_t c = lane; c < nch; c += 32) copy(c);
       }
       if (SOA && lane == 31) {
         const uint64_t r2 = static_cast<uint64_t>(r) & ~1ull;
-        const uint32_t bytes = (r2 + 1 < p.n_rows) ? 4u : 2u;
-        cp_async4(sb + p.alpha_slot, p.alpha + r2, bytes);
+        // alpha_slot is measured from the stage start, like the decode's read
+        cp_async4(sa - kStagePrefix + p.alpha_slot, p.alpha + r2, (r2 + 1 < n_rows) ? 4u : 2u);
       }
       m = 1u | ((static_cast<uint32_t>(r) & 1u) << 1) | (mis << 8);
     } else if (lane == 0) {
       atomicOr(p.status, 1u);
     }
-    if (lane == 0) meta[st] = m;
+    if (lane == 0) {
+      meta[2 * st] = m;
+      if (PERM) meta[2 * st + 1] = jrow;
+    }
     cp_async_commit();
   };
 
 #pragma unroll
   for (int q = 0; q < PF - 1; ++q) {
-    if (static_cast<uint64_t>(q) < cnt) issue(q);
+    if (static_cast<uint32_t>(q) < cnt) issue(q);
     else cp_async_commit();
   }
 
-  for (uint64_t i = 0; i < cnt; ++i) {
-    const uint64_t q = i + PF - 1;
-    if (q < cnt) issue(q);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint4* orow_seq = reinterpret_cast<uint4*>(p.out) + lo * (d >> 3);
+  for (uint32_t i = 0; i < cnt; ++i, orow_seq += (d >> 3)) {
+    if (i + PF - 1 < cnt) issue(i + PF - 1);
     else cp_async_commit();
     cp_async_wait<PF - 1>();
     __syncwarp();
 
-    const uint32_t st = static_cast<uint32_t>(i % PF);
-    const uint8_t* sb = stages + st * p.stage_bytes;
-    const uint32_t m = meta[st];
-    uint4* orow = reinterpret_cast<uint4*>(p.out) + (lo + i) * C;
+    const uint32_t st = i & (PF - 1);
+    uint8_t* sb = stages + st * stage_bytes + kStagePrefix;
+    const uint32_t m = meta[2 * st];
+    uint4* orow = PERM ? reinterpret_cast<uint4*>(p.out) +
+                             static_cast<uint64_t>(meta[2 * st + 1]) * (d >> 3)
+                       : orow_seq;
     if (m & 1u) {
       const uint32_t mis = m >> 8;
-      uint16_t abits;
-      if (SOA) abits = *reinterpret_cast<const uint16_t*>(sb + p.alpha_slot + 2 * ((m >> 1) & 1u));
-      else abits = *reinterpret_cast<const uint16_t*>(sb + mis + p.code_bytes);
+      uint8_t* code = sb + mis;
+      // Tail-biting splice: the code's last 16 bits just below bit 0.
+      if (lane == 0)
+        *reinterpret_cast<uint16_t*>(code - 2) =
+            *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+      const uint16_t abits = SOA ? *reinterpret_cast<const uint16_t*>(
+                                       sb - kStagePrefix + p.alpha_slot + 2 * ((m >> 1) & 1u))
+                                 : *reinterpret_cast<const uint16_t*>(code + code_bytes);
+      __syncwarp();
       const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(sb);
-      const uint32_t boff = mis * 8;
-      for (uint32_t c = lane; c < C; c += 32) {
-        const int32_t pb = K * static_cast<int32_t>(4 * c + 1) - 16;
-        uint64_t x;
-        if (pb >= 0) {
-          x = bits64(w, boff + static_cast<uint32_t>(pb));
-        } else {                                        // tail-biting wrap
-          const uint32_t nt = static_cast<uint32_t>(-pb);
-          const uint64_t tail = bits64(w, boff + Lc - nt) & ((1ull << nt) - 1);
-          x = tail | (bits64(w, boff) << nt);
-        }
-        st_stream(orow + c, decode_chunk<K>(x, lut_lane, a));
+      const uint32_t ex = (abits >> 7) & 0xFFu;
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(sb - kStagePrefix);
+      const uint32_t boff = (kStagePrefix + mis) * 8;
+      if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {   // |alpha| in [2^-14, 2^16) or 0
+        const __half ah = __float2half_rn(a);             // exact in this range
+        decode_row<K, CPL, true>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
+      } else {
+        decode_row<K, CPL, false>(w, boff, d, smem, lane, 0, a, orow);
       }
     } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (uint32_t c = lane; c < C; c += 32) st_stream(orow + c, z);
+      for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
     }
     __syncwarp();
   }

@@ -149,6 +149,39 @@ cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t 
  */
 cp_status cp_get_status(const cp_table* t, void* stream);
 
+/*
+ * cp_lookup_decode_host_noalloc -- cp_lookup_decode_host for callers that
+ * cannot allocate device memory.  (The pages have no counterpart: this is an
+ * integration entry point of this library.)
+ *
+ * Who needs it: code whose device memory belongs to one pool allocator (a
+ * plugin may not call cudaMalloc behind the owner's back), code that must not
+ * call cudaMalloc/cudaFree while other streams run (both can synchronise the
+ * device), or a runtime that fixes its memory budget up front.  cp_table_load
+ * allocates, so such callers pass everything themselves:
+ *   records   pinned, mapped host memory holding n_rows AoS records (16-byte
+ *             aligned; page-locked by the caller, e.g. cudaHostAlloc).
+ *   n_rows, d, bits_per_step: geometry as for cp_table_load.
+ *   lut_fp16  host pointer, 512 x (y0, y1) fp16 patterns, finite.
+ *   idx       device, n int64 ids;  out: device bf16 [n][d], 16-byte aligned.
+ *   status    device uint32 owned by the caller: bit 0 is OR-ed in when an id is
+ *             out of range (clear it yourself before the call if needed).
+ * It allocates nothing: its scratch (the LUT copy, the dedupe table, the visiting
+ * order) is one static device array of about 2 MB that every GPU loading the
+ * library holds until the process exits.  Limit: n <= 65536 lookups per call;
+ * larger n returns CP_ERR_INVALID_ARG before any work is queued.
+ * The first call on a device looks up that array's device address (once per
+ * device); make that first call before any stream capture.  All calls share the
+ * array and it keeps the last call's contents (each call clears what must start
+ * empty), so calls that overlap on the GPU (on different streams, or from
+ * different threads without ordering) race: order them on one stream.
+ * The output equals cp_lookup_decode_host's bit for bit.
+ */
+cp_status cp_lookup_decode_host_noalloc(const void* records, uint64_t n_rows, uint32_t d,
+                                        uint32_t bits_per_step, const uint16_t* lut_fp16,
+                                        const int64_t* idx, uint64_t n, uint16_t* out,
+                                        uint32_t* status, void* stream);
+
 /* Release what the handle owns (LUT copy, status word, host registration made
  * by cp_table_load).  Borrowed buffers are untouched.  NULL is a no-op. */
 void cp_table_free(cp_table* t);

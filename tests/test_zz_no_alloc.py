@@ -1,0 +1,65 @@
+"""cp_lookup_decode_host_noalloc: the host-resident decode for callers that cannot
+allocate device memory (its scratch is a static device array inside libcp).
+
+Collected last on purpose.  It must agree bit for bit with cp_lookup_decode_host
+(the tolerance of every parity test here), on two calls in a row that share the
+static scratch, whether run alone or after the other tests.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import trellis_row_decode_gb300 as cp
+from trellis_row_decode_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy()
+
+
+def test_noalloc_matches_table_entry_point_on_consecutive_calls():
+    d, k, n_rows = 1024, 4, 20011
+    rec = synth.gen_records(11, torch.arange(n_rows), d, k).reshape(-1).contiguous().pin_memory()
+    table = cp.load_table(rec, n_rows, d, k)            # the existing host-resident entry point
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    free_before = None
+    for call, (seed, n) in enumerate([(5, 40000), (6, 65536)]):
+        idx_np = synth.zipf_indices(seed, n, n_rows)
+        idx_np[3] = -1                                   # one out-of-range id per call
+        idx = torch.from_numpy(idx_np).cuda()
+        ref = cp.lookup_decode_host(table, idx)
+        assert cp.get_status(table) == cp.CP_ERR_INDEX_OOB
+        status.zero_()
+        out = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+        if call == 1:
+            torch.cuda.synchronize()
+            free_before = torch.cuda.mem_get_info()[0]
+        cp.lookup_decode_host_noalloc(rec, n_rows, d, k, idx, out, status)
+        torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] >= free_before - (2 << 20)
+        assert np.array_equal(_bits(out), _bits(ref)), f"call {call}: output differs"
+        assert int(status.item()) & 1 == 1
+        assert not out[3].view(torch.int16).any()
+    table.close()
+
+
+def test_noalloc_rejects_more_than_its_capacity():
+    d, k, n_rows = 256, 4, 100
+    rec = synth.gen_records(1, torch.arange(n_rows), d, k).reshape(-1).contiguous().pin_memory()
+    n = 65537
+    idx = torch.zeros(n, dtype=torch.int64, device="cuda")
+    out = torch.full((n, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lut = cp.default_lut()
+    rc = cp.lib().cp_lookup_decode_host_noalloc(rec.data_ptr(), n_rows, d, k, lut.ctypes.data,
+                                                idx.data_ptr(), n, out.data_ptr(),
+                                                status.data_ptr(), None)
+    assert rc == cp.CP_ERR_INVALID_ARG
+    assert b"65536" in cp.lib().cp_last_error()
+    torch.cuda.synchronize()
+    assert bool((out.float() == 3.0).all())              # nothing was queued

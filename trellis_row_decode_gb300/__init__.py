@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
-    "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH",
+    "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -73,6 +73,8 @@ def lib():
         L.cp_last_error.argtypes = []
         L.cp_test_inject_failure.restype = i32
         L.cp_test_inject_failure.argtypes = [i32, i32]
+        L.cp_lookup_decode_host_noalloc.restype = i32
+        L.cp_lookup_decode_host_noalloc.argtypes = [vp, u64, u32, u32, vp, vp, u64, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -179,3 +181,32 @@ def lookup_decode_host(table: Table, idx: torch.Tensor, out: torch.Tensor | None
 def get_status(table: Table, stream=None) -> int:
     """Synchronise the stream; CP_ERR_INDEX_OOB if an id was out of range since the last call."""
     return int(lib().cp_get_status(table.handle, _stream_ptr(stream)))
+
+
+def lookup_decode_host_noalloc(records: torch.Tensor, n_rows: int, d: int, k: int,
+                               idx: torch.Tensor, out: torch.Tensor, status: torch.Tensor,
+                               lut: np.ndarray | None = None, stream=None) -> torch.Tensor:
+    """Host-resident decode that allocates no device memory in the library.
+
+    For callers that cannot allocate device memory themselves at decode time:
+    `records` (pinned host uint8), `out` (bf16 [n, d]) and `status` (one int32 on
+    the device, bit 0 set for out-of-range ids) are all provided by the caller;
+    at most 65,536 lookups per call.  Calls that overlap on the GPU race on the
+    library's static scratch: order them on one stream.
+    """
+    if records.is_cuda or records.dtype != torch.uint8 or not records.is_contiguous():
+        raise ValueError("records must be a contiguous pinned uint8 host tensor")
+    if idx.dtype != torch.int64 or not idx.is_cuda or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int64 CUDA tensor")
+    if out.dtype != torch.bfloat16 or out.shape != (idx.numel(), d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of shape (n, d)")
+    if status.dtype != torch.int32 or not status.is_cuda:
+        raise ValueError("status must be an int32 CUDA tensor")
+    if lut is None:
+        lut = default_lut()
+    lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    st = lib().cp_lookup_decode_host_noalloc(records.data_ptr(), n_rows, d, k, lut.ctypes.data,
+                                             idx.data_ptr(), idx.numel(), out.data_ptr(),
+                                             status.data_ptr(), _stream_ptr(stream))
+    _check(st, "cp_lookup_decode_host_noalloc")
+    return out

@@ -11,32 +11,7 @@
 
 #include "cp.h"
 #include "cp_dispatch.h"
-
-struct cp_table {
-  int device;
-  int residency;
-  int layout;
-  uint64_t n_rows;
-  uint32_t d;
-  uint32_t k;
-  uint32_t rec_bytes;     // R
-  uint32_t code_bytes;    // d*k/16
-  uint32_t soa_stride;    // S
-  const uint8_t* rec;     // device-accessible AoS records (HBM, or alias of host memory)
-  const uint8_t* soa_codes;
-  const uint16_t* soa_alpha;
-  uint32_t* lut_dev;      // 512 words
-  uint32_t* status_dev;   // 1 word
-  void* scratch_dev;      // host-resident tables: dedupe keys (kHashSlotsMax x 8 B),
-                          // owners (kHashSlotsMax), dup (kBucketChunk), bucket counts
-                          // (nb + 1, padded), visiting order (kBucketChunk)
-  uint32_t bucket_shift;  // bucket of row r = r >> bucket_shift
-  uint32_t bucket_nb;     // number of row-range buckets
-  void* registered;       // host range this handle registered, else nullptr
-  int sm_count;
-  int max_smem;           // opt-in shared memory per block
-  cpk::KernelSet kernels;
-};
+#include "cp_internal.h"
 
 namespace {
 
@@ -44,20 +19,41 @@ thread_local std::string g_last_error;
 std::atomic<int> g_fail_alloc{0};
 std::atomic<int> g_fail_register{0};
 
-constexpr uint64_t kMaxRows = 1ull << 40;
-constexpr uint64_t kMaxLookups = 1ull << 40;
-
-cp_status cuda_fail(cudaError_t e, const char* what) {
-  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
-  return CP_ERR_CUDA;
-}
-
 bool take_injected(std::atomic<int>& c) {
   int v = c.load();
   while (v > 0) {
     if (c.compare_exchange_weak(v, v - 1)) return true;
   }
   return false;
+}
+
+}  // namespace
+
+namespace cpx {
+
+void set_error(const std::string& what) { g_last_error = what; }
+
+cp_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return CP_ERR_CUDA;
+}
+
+HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb) {
+  HostScratch h;
+  h.capacity = capacity;
+  h.keys = static_cast<unsigned long long*>(base);
+  h.owner = reinterpret_cast<uint32_t*>(h.keys + 2ull * capacity);
+  h.dup = h.owner + 2ull * capacity;
+  h.counts = h.dup + capacity;
+  h.perm = h.counts + ((nb + 1 + 63) & ~63u);
+  return h;
+}
+
+void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb) {
+  uint32_t bits = 0;
+  while (bits < 64 && ((n_rows - 1) >> bits) != 0) ++bits;
+  *shift = bits > cpk::kBucketBits ? bits - cpk::kBucketBits : 0;
+  *nb = static_cast<uint32_t>(((n_rows - 1) >> *shift) + 1);
 }
 
 bool geometry_ok(uint32_t d, uint32_t k) {
@@ -97,7 +93,7 @@ uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot) {
 }
 
 cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
-                        cudaStream_t stream, bool host_path) {
+                        cudaStream_t stream, bool host_path, const HostScratch* hs) {
   const bool soa = (t->layout == CP_LAYOUT_SOA);
   const int pf = host_path ? cpk::kPfHost : cpk::kPfDevice;
   const int ci = cpk::cpl_index(t->d);
@@ -148,17 +144,18 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
     return CP_OK;
   }
-  // Host-resident table, per pass of at most kBucketChunk lookups: elect one
+  // Host-resident table, per pass of at most hs->capacity lookups: elect one
   // owner per distinct id, partition the owners by row range, decode them in
   // that order (each row lands at its own position), then fill the other
   // lookups from their owner's row.
-  unsigned long long* keys = static_cast<unsigned long long*>(t->scratch_dev);
-  uint32_t* owner = reinterpret_cast<uint32_t*>(keys + cpk::kHashSlotsMax);
-  uint32_t* dup = owner + cpk::kHashSlotsMax;
-  uint32_t* counts = dup + cpk::kBucketChunk;
-  uint32_t* perm = counts + ((t->bucket_nb + 1 + 63) & ~63u);
-  for (uint64_t c0 = 0; c0 < n; c0 += cpk::kBucketChunk) {
-    const uint64_t m = (n - c0 < cpk::kBucketChunk) ? n - c0 : cpk::kBucketChunk;
+  unsigned long long* keys = hs->keys;
+  uint32_t* owner = hs->owner;
+  uint32_t* dup = hs->dup;
+  uint32_t* counts = hs->counts;
+  uint32_t* perm = hs->perm;
+  const uint64_t cap = hs->capacity;
+  for (uint64_t c0 = 0; c0 < n; c0 += cap) {
+    const uint64_t m = (n - c0 < cap) ? n - c0 : cap;
     uint32_t ts = 1024;
     while (ts < 2 * m) ts <<= 1;
     e = cudaMemsetAsync(keys, 0, ts * sizeof(unsigned long long), stream);
@@ -188,6 +185,18 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   return CP_OK;
 }
 
+}  // namespace cpx
+
+namespace {
+
+using cpx::aligned;
+using cpx::cuda_fail;
+using cpx::geometry_ok;
+using cpx::kernels_for;
+using cpx::kMaxLookups;
+using cpx::kMaxRows;
+using cpx::soa_stride;
+
 cp_status decode_common(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                         void* stream, int want_residency) {
   if (t == nullptr) return CP_ERR_INVALID_ARG;
@@ -209,8 +218,11 @@ cp_status decode_common(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     g_last_error = "current device differs from the table's device";
     return CP_ERR_INVALID_ARG;
   }
-  return launch_decode(t, idx, n, out, static_cast<cudaStream_t>(stream),
-                       want_residency == CP_RESIDENT_HOST);
+  const bool host = want_residency == CP_RESIDENT_HOST;
+  cpx::HostScratch hs{};
+  if (host) hs = cpx::host_scratch_layout(t->scratch_dev, cpk::kBucketChunk, t->bucket_nb);
+  return cpx::launch_decode(t, idx, n, out, static_cast<cudaStream_t>(stream), host,
+                            host ? &hs : nullptr);
 }
 
 }  // namespace
@@ -345,13 +357,8 @@ cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, ui
   const uint64_t table_bytes = n_rows * t->rec_bytes;
   if (residency == CP_RESIDENT_HOST) {
     // row-range buckets of the visiting order: at most 2^kBucketBits of them
-    uint32_t bits = 0;
-    while (bits < 64 && ((n_rows - 1) >> bits) != 0) ++bits;
-    t->bucket_shift = bits > cpk::kBucketBits ? bits - cpk::kBucketBits : 0;
-    t->bucket_nb = static_cast<uint32_t>(((n_rows - 1) >> t->bucket_shift) + 1);
-    const size_t bytes = cpk::kHashSlotsMax * (sizeof(unsigned long long) + sizeof(uint32_t)) +
-                         (static_cast<size_t>(cpk::kBucketChunk) * 2 +
-                          ((t->bucket_nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
+    cpx::bucket_params(n_rows, &t->bucket_shift, &t->bucket_nb);
+    const size_t bytes = cpx::host_scratch_bytes(cpk::kBucketChunk, t->bucket_nb);
     if (take_injected(g_fail_alloc)) {
       g_last_error = "injected device allocation failure";
       cp_table_free(t);

@@ -1,0 +1,75 @@
+// cp_internal.h -- host-side internals shared by the C ABI translation units.
+#pragma once
+
+#include <cstdint>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "cp.h"
+#include "cp_dispatch.h"
+
+struct cp_table {
+  int device;
+  int residency;
+  int layout;
+  uint64_t n_rows;
+  uint32_t d;
+  uint32_t k;
+  uint32_t rec_bytes;     // R
+  uint32_t code_bytes;    // d*k/16
+  uint32_t soa_stride;    // S
+  const uint8_t* rec;     // device-accessible AoS records (HBM, or alias of host memory)
+  const uint8_t* soa_codes;
+  const uint16_t* soa_alpha;
+  uint32_t* lut_dev;      // 512 words
+  uint32_t* status_dev;   // 1 word
+  void* scratch_dev;      // host-resident tables: see cpx::HostScratch (kBucketChunk capacity)
+  uint32_t bucket_shift;  // bucket of row r = r >> bucket_shift
+  uint32_t bucket_nb;     // number of row-range buckets
+  void* registered;       // host range this handle registered, else nullptr
+  int sm_count;
+  int max_smem;           // opt-in shared memory per block
+  cpk::KernelSet kernels;
+};
+
+namespace cpx {
+
+constexpr uint64_t kMaxRows = 1ull << 40;
+constexpr uint64_t kMaxLookups = 1ull << 40;
+
+// Device scratch of the host-resident path for passes of up to `capacity`
+// lookups: the dedupe table (2 * capacity slots of 64-bit keys and 32-bit
+// owners), the owner of each lookup, the bucket counts and the visiting order.
+struct HostScratch {
+  unsigned long long* keys;
+  uint32_t* owner;
+  uint32_t* dup;
+  uint32_t* counts;
+  uint32_t* perm;
+  uint32_t capacity;
+};
+
+constexpr size_t host_scratch_bytes(uint32_t capacity, uint32_t nb) {
+  return static_cast<size_t>(2) * capacity * (sizeof(unsigned long long) + sizeof(uint32_t)) +
+         (static_cast<size_t>(2) * capacity + ((nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
+}
+
+HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb);
+
+// Bucket shift and count for n_rows rows: at most 2^kBucketBits ranges.
+void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb);
+
+bool geometry_ok(uint32_t d, uint32_t k);
+uint32_t soa_stride(uint32_t d, uint32_t k);
+bool aligned(const void* p, uintptr_t a);
+cpk::KernelSet kernels_for(uint32_t k);
+void set_error(const std::string& what);
+cp_status cuda_fail(cudaError_t e, const char* what);
+
+// Queue one lookup-decode on `stream`.  host_path: the owner/partition pipeline
+// of host-resident tables, run in passes of hs->capacity lookups.
+cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                        cudaStream_t stream, bool host_path, const HostScratch* hs);
+
+}  // namespace cpx

@@ -9,7 +9,11 @@ read that flush the 129 MB L2, so no step reuses the previous step's records
 from L2 and no dirty flush lines are written back inside the next step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--layout aos|soa] [--host-path]
+                  [--impl ours|reference] [--layout aos|soa] [--no-host-path]
+
+The same run also times cp_lookup_decode_host on the same table placed in
+pinned host DRAM ("host_path" in the JSON line, against the measured
+host-to-device copy bandwidth), unless --no-host-path.
 
 Under torchrun (N > 1) every rank holds its own replica of the table and
 decodes its own replay (seed + rank); no collective touches the data path
@@ -51,8 +55,8 @@ def parse():
     ap.add_argument("--workload", default="deepseek_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layout", default="aos", choices=["aos", "soa"])
-    ap.add_argument("--host-path", action="store_true",
-                    help="also time cp_lookup_decode_host on the table in pinned host DRAM")
+    ap.add_argument("--no-host-path", action="store_true",
+                    help="skip timing cp_lookup_decode_host on the table in pinned host DRAM")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -264,6 +268,21 @@ def time_steps(fn, steps, warmup, flush, stream):
     return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
 
 
+def aggregate(local_time_s: float, local_units: int, world: int, dist, device):
+    """Max of the ranks' timed totals and the whole-job throughput.
+
+    Every rank processes `local_units` in `local_time_s`; the job takes as long as
+    its slowest rank, so value = local_units * world / max_rank(time).
+    """
+    total = local_time_s
+    if dist is not None and world > 1:
+        import torch
+        tt = torch.tensor([total], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total = float(tt.item())
+    return total, local_units * world / total
+
+
 def our_arm(args, w, rank, world, local):
     import torch
     import trellis_row_decode_gb300 as cp
@@ -293,12 +312,7 @@ def our_arm(args, w, rank, world, local):
         dist.barrier()
     status = cp.get_status(table)
     assert status == cp.CP_OK, status
-    total = float(t.sum())
-    if dist is not None:
-        tt = torch.tensor([total], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total = float(tt.item())
-    value = n * args.steps * world / total
+    total, value = aggregate(float(t.sum()), n * args.steps, world, dist, "cuda")
     mean_t = total / args.steps
     bpl = w.algorithmic_bytes_per_lookup()
     achieved = n * bpl / float(t.mean()) / 1e9
@@ -319,7 +333,11 @@ def our_arm(args, w, rank, world, local):
     e2e_value = n / float(te.mean())
 
     host_obj = None
-    if args.host_path:
+    if not args.no_host_path and rank == 0 and w.residency in ("device", "host") \
+            and w.d >= 256:
+        del rec, soa
+        table.close()
+        torch.cuda.empty_cache()
         host_obj = host_path_measure(args, w, idx, flush, stream)
 
     cpu = None
@@ -392,12 +410,19 @@ def host_path_measure(args, w, idx, flush, stream):
     table = cp.load_table(host, w.n_rows, w.d, w.k, cp.default_lut())
     n = idx.numel()
     out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
-    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), 20, 3, flush, stream)
+    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), 50, 3, flush, stream)
     assert cp.get_status(table) == cp.CP_OK
-    link_gbs = n * R / float(np.median(t)) / 1e9
+    tm = float(np.median(t))
+    link_gbs = n * R / tm / 1e9
+    uniq = int(torch.unique(idx).numel())
     table.close()
-    return {"ms_per_step": float(np.median(t) * 1e3), "rows_per_s": n / float(np.median(t)),
-            "record_gbs": link_gbs, "h2d_measured_gbs": h2d, "frac_of_h2d": link_gbs / h2d}
+    return {"entry_point": "cp_lookup_decode_host", "table": "pinned host DRAM",
+            "ms_per_step": tm * 1e3, "rows_per_s": n / tm,
+            "bound": "host link", "achieved": link_gbs, "unit": "GB/s",
+            "peak": h2d, "peak_kind": "measured (cudaMemcpyAsync pinned->device, 1 GB)",
+            "frac": link_gbs / h2d,
+            "bytes_per_lookup": R, "unique_ids": uniq,
+            "unique_record_gbs": uniq * R / tm / 1e9}
 
 
 def main():

@@ -114,10 +114,13 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   p.out = out;
   p.status = t->status_dev;
 
-  int nwarps = cpk::kMaxWarps;
+  const bool reg_ring = host_path && cpk::host_uses_register_ring(ci);
+  int nwarps = reg_ring ? cpk::kHostWarps : cpk::kMaxWarps;
+  const size_t lut = cpk::lut_bytes(reg_ring ? 32 : (host_path ? cpk::kLutRepHost
+                                                               : cpk::kLutRepDevice));
   auto smem_for = [&](int w) {
-    return static_cast<size_t>(cpk::kLutBytes) + static_cast<size_t>(w) * pf * p.stage_bytes +
-           static_cast<size_t>(w) * pf * 8;
+    if (reg_ring) return lut + static_cast<size_t>(w) * p.stage_bytes;   // one stage per warp
+    return lut + static_cast<size_t>(w) * pf * p.stage_bytes + static_cast<size_t>(w) * pf * 8;
   };
   while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
   const size_t smem = smem_for(nwarps);

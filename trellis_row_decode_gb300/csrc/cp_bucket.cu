@@ -40,30 +40,48 @@ __device__ __forceinline__ bool visits(const uint32_t* dup, uint64_t j) {
 
 // dup[j] = the owner lookup of idx[j] (the first to claim the id's slot in an
 // open-addressing table of ts = 2^k slots, keys r + 1, 0 = empty), or kNoOwner
-// for an id outside [0, n_rows).  Probing is bounded by ts; a lookup that
-// finds no slot owns itself (still correct, just not deduplicated).
+// for an id outside [0, n_rows).  Lanes of a warp holding the same id share one
+// probe (the group's lowest lane probes); slots are read before any CAS, so the
+// lookups of a hot id do not serialise on one atomic.  Probing is bounded by ts;
+// a lookup that finds no slot owns itself (still correct, just not deduplicated).
 __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint64_t n_rows,
                               unsigned long long* __restrict__ keys, uint32_t* __restrict__ owner,
                               uint32_t ts, uint32_t* __restrict__ dup) {
-  const uint64_t T = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n; j += T) {
-    const int64_t r = __ldg(idx + j);
-    if (static_cast<uint64_t>(r) >= n_rows) {
-      dup[j] = kNoOwner;
-      continue;
-    }
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
+       base < n; base += warps * 32) {
+    const uint64_t j = base + lane;
+    const int64_t r = (j < n) ? __ldg(idx + j) : -1;
+    const bool valid = j < n && static_cast<uint64_t>(r) < n_rows;
+    if (j < n && !valid) dup[j] = kNoOwner;
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    if (!valid) continue;
     const unsigned long long key = static_cast<unsigned long long>(r) + 1ull;
-    uint32_t slot = static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
+    const uint32_t group = __match_any_sync(active, key);
+    const uint32_t leader = __ffs(group) - 1;
     uint32_t o = static_cast<uint32_t>(j);
-    for (uint32_t probe = 0; probe < ts; ++probe) {
-      const unsigned long long prev = atomicCAS(keys + slot, 0ull, key);
-      if (prev == 0ull || prev == key) {
-        const uint32_t w = atomicCAS(owner + slot, kNoOwner, static_cast<uint32_t>(j));
-        o = (w == kNoOwner) ? static_cast<uint32_t>(j) : w;
-        break;
+    if (lane == leader) {
+      uint32_t slot = static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
+      for (uint32_t probe = 0; probe < ts; ++probe) {
+        unsigned long long cur = __ldcg(keys + slot);
+        if (cur == 0ull) {
+          cur = atomicCAS(keys + slot, 0ull, key);
+          if (cur == 0ull) cur = key;
+        }
+        if (cur == key) {
+          uint32_t w = __ldcg(owner + slot);
+          if (w == kNoOwner) {
+            w = atomicCAS(owner + slot, kNoOwner, static_cast<uint32_t>(j));
+            if (w == kNoOwner) w = static_cast<uint32_t>(j);
+          }
+          o = w;
+          break;
+        }
+        slot = (slot + 1) & (ts - 1);
       }
-      slot = (slot + 1) & (ts - 1);
     }
+    o = __shfl_sync(group, o, leader);
     dup[j] = o;
   }
 }
@@ -161,7 +179,7 @@ __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, const uin
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
                    uint32_t* owner, uint32_t ts, uint32_t* dup, int sm_count, cudaStream_t s) {
   dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(idx, n, n_rows, keys, owner, ts,
-                                                                     dup);
+                                                                     dup);  // warp-strided
 }
 
 void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,

@@ -5,23 +5,29 @@
 namespace cpk {
 
 namespace {
-template <bool SOA, int PF, bool PERM>
+template <bool SOA, int PF, bool PERM, int REP>
 void fill(DecodeFn* row) {
-  row[0] = &lookup_decode_kernel<3, SOA, PF, 0, PERM>;
-  row[1] = &lookup_decode_kernel<3, SOA, PF, 1, PERM>;
-  row[2] = &lookup_decode_kernel<3, SOA, PF, 2, PERM>;
-  row[3] = &lookup_decode_kernel<3, SOA, PF, 4, PERM>;
-  row[4] = &lookup_decode_kernel<3, SOA, PF, 8, PERM>;
-  row[5] = &lookup_decode_kernel<3, SOA, PF, 16, PERM>;
+  row[0] = &lookup_decode_kernel<3, SOA, PF, 0, PERM, REP>;
+  row[1] = &lookup_decode_kernel<3, SOA, PF, 1, PERM, REP>;
+  row[2] = &lookup_decode_kernel<3, SOA, PF, 2, PERM, REP>;
+  row[3] = &lookup_decode_kernel<3, SOA, PF, 4, PERM, REP>;
+  row[4] = &lookup_decode_kernel<3, SOA, PF, 8, PERM, REP>;
+  row[5] = &lookup_decode_kernel<3, SOA, PF, 16, PERM, REP>;
 }
 }  // namespace
 
 KernelSet kernels_k3() {
   KernelSet s;
-  fill<false, kPfDevice, false>(s.dev[0]);
-  fill<true, kPfDevice, false>(s.dev[1]);
-  fill<false, kPfHost, true>(s.host[0]);
-  fill<true, kPfHost, true>(s.host[1]);
+  fill<false, kPfDevice, false, kLutRepDevice>(s.dev[0]);
+  fill<true, kPfDevice, false, kLutRepDevice>(s.dev[1]);
+  fill<false, kPfHost, true, kLutRepHost>(s.host[0]);
+  fill<true, kPfHost, true, kLutRepHost>(s.host[1]);
+  s.host[0][1] = &lookup_decode_host_kernel<3, false, kPfHostReg, 1, 32>;
+  s.host[0][2] = &lookup_decode_host_kernel<3, false, kPfHostReg, 2, 32>;
+  s.host[0][3] = &lookup_decode_host_kernel<3, false, kPfHostReg, 4, 32>;
+  s.host[1][1] = &lookup_decode_host_kernel<3, true, kPfHostReg, 1, 32>;
+  s.host[1][2] = &lookup_decode_host_kernel<3, true, kPfHostReg, 2, 32>;
+  s.host[1][3] = &lookup_decode_host_kernel<3, true, kPfHostReg, 4, 32>;
   return s;
 }
 

@@ -11,10 +11,15 @@ namespace cpk {
 #define CP_PF_DEVICE 2
 #endif
 #ifndef CP_PF_HOST
-#define CP_PF_HOST 8
+#define CP_PF_HOST 16
+#endif
+#ifndef CP_LUTREP_HOST
+#define CP_LUTREP_HOST 4
 #endif
 constexpr int kPfDevice = CP_PF_DEVICE;
 constexpr int kPfHost = CP_PF_HOST;
+constexpr int kLutRepDevice = 32;
+constexpr int kLutRepHost = CP_LUTREP_HOST;
 
 using DecodeFn = void (*)(DecodeParams);
 
@@ -31,8 +36,14 @@ inline int cpl_index(uint32_t d) {
 
 struct KernelSet {
   DecodeFn dev[2][kCplVariants];    // [layout AoS/SoA][cpl index], lookup order
-  DecodeFn host[2][kCplVariants];   // bucketed order (PERM)
+  DecodeFn host[2][kCplVariants];   // bucketed order: register-ring kernel for cpl
+                                    // indices 1..3 (d <= 1024), cp.async kernel otherwise
 };
+
+// Host-path kernels for cpl indices 1..3 are lookup_decode_host_kernel (one
+// shared stage per warp, kHostWarps warps per CTA).
+inline bool host_uses_register_ring(int cpl_idx) { return cpl_idx >= 1 && cpl_idx <= 3; }
+constexpr int kPfHostReg = 8;
 
 // Host-resident tables: lookups are visited bucketed by row-id range so that
 // consecutive records of a warp are close in the host address space.

@@ -16,7 +16,10 @@
 //   * the shared LUT (512 fp16 pairs) is expanded in shared memory to 1024
 //     entries (the sign of y1 folded in, indexed by hash bits 14..23) and
 //     replicated 32 times, word (entry * 32 + lane): every lane reads its own
-//     bank, so a warp-wide LUT read is one wavefront;
+//     bank, so a warp-wide LUT read is one wavefront.  The host-resident
+//     variant is bound by the host link, whose throughput here grows with the
+//     bytes in flight; it keeps 4 replicas (16 KB) and spends the shared memory
+//     on a deeper record ring instead;
 //   * a record lands 16 bytes into its stage; once it has arrived, lane 0 copies
 //     the code's last 16 bits (a whole halfword, since d*k/16 is even) to the
 //     two bytes just below code bit 0, so the tail-biting wrap (windows that
@@ -44,8 +47,10 @@
 namespace cpk {
 
 constexpr int kLutEntries = 1024;                  // 512 pairs x sign of y1
-constexpr int kLutReplicas = 32;                   // one per lane / bank
-constexpr int kLutBytes = kLutEntries * kLutReplicas * 4;   // 128 KB
+// Shared-memory LUT bytes with REP replicas (REP = 32: one per lane, no bank
+// conflicts, 128 KB; REP = 4: 16 KB, leaving room for more record stages).
+constexpr int lut_bytes(int rep) { return kLutEntries * rep * 4; }
+constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 #ifndef CP_MAX_WARPS
 #define CP_MAX_WARPS 32
 #endif
@@ -115,22 +120,25 @@ __device__ __forceinline__ uint32_t scale_pair_f32(uint32_t v, float a) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// LUT word of state s for this lane: byte offset ((h >> 14) & 1023) * 128 + lane * 4.
-__device__ __forceinline__ uint32_t lut_word(const uint8_t* lut_bytes, uint32_t s, uint32_t lane4) {
+// LUT word of state s for this lane: entry e = (h >> 14) & 1023 at byte offset
+// e * REP * 4, replica (lane % REP); lane4 = (lane % REP) * 4.
+template <int REP>
+__device__ __forceinline__ uint32_t lut_word(const uint8_t* lut, uint32_t s, uint32_t lane4) {
+  constexpr int kSh = log2i(REP * 4);                             // 7 for REP = 32
   const uint32_t h = s * s + s;                                   // mod 2^32
-  const uint32_t off = ((h >> 7) & ((kLutEntries - 1) << 7)) | lane4;
-  return *reinterpret_cast<const uint32_t*>(lut_bytes + off);
+  const uint32_t off = ((h >> (14 - kSh)) & ((kLutEntries - 1) << kSh)) | lane4;
+  return *reinterpret_cast<const uint32_t*>(lut + off);
 }
 
 // Steps 4c..4c+3 of a row from x (bit 0 = first bit of the first window).
-template <int K, bool F16>
-__device__ __forceinline__ uint4 decode_chunk(uint64_t x, const uint8_t* lut_bytes,
+template <int K, bool F16, int REP>
+__device__ __forceinline__ uint4 decode_chunk(uint64_t x, const uint8_t* lut,
                                               uint32_t lane4, uint16_t a_h, float a) {
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t s = static_cast<uint32_t>(x >> (K * j)) & 0xFFFFu;
-    const uint32_t v = lut_word(lut_bytes, s, lane4);
+    const uint32_t v = lut_word<REP>(lut, s, lane4);
     o[j] = F16 ? scale_pair_f16(v, a_h) : scale_pair_f32(v, a);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -143,11 +151,11 @@ __device__ __forceinline__ uint64_t funnel64(uint32_t lo, uint32_t hi, uint32_t 
 // Decode one staged row into orow (16-byte chunks).  w: staged words; boff: bit
 // offset of code bit 0 in the stage (>= 16 bits of spliced tail below it).
 // CPL > 0: d == 256 * CPL.
-template <int K, int CPL, bool F16>
+template <int K, int CPL, bool F16, int REP>
 __device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uint32_t d,
                                            const uint8_t* lut_bytes, uint32_t lane,
                                            uint16_t a_h, float a, uint4* orow) {
-  const uint32_t lane4 = lane << 2;
+  const uint32_t lane4 = (lane & (REP - 1)) << 2;
   if constexpr (CPL > 0) {
     // chunk c = lane + 32 m starts at bit boff + K(4 lane + 1) - 16 + 128 K m
     const uint32_t P0 = boff + K * (4 * lane + 1) - 16;
@@ -156,14 +164,14 @@ __device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uin
 #pragma unroll
     for (int m = 0; m < CPL; ++m) {
       const uint64_t x = funnel64(w0[4 * K * m], w0[4 * K * m + 1], sh);
-      __stcs(orow + lane + 32 * m, decode_chunk<K, F16>(x, lut_bytes, lane4, a_h, a));
+      __stcs(orow + lane + 32 * m, decode_chunk<K, F16, REP>(x, lut_bytes, lane4, a_h, a));
     }
   } else {
     const uint32_t C = d >> 3;
     for (uint32_t c = lane; c < C; c += 32) {
       const uint32_t P = boff + K * (4 * c + 1) - 16;
       const uint64_t x = funnel64(w[P >> 5], w[(P >> 5) + 1], P & 31);
-      __stcs(orow + c, decode_chunk<K, F16>(x, lut_bytes, lane4, a_h, a));
+      __stcs(orow + c, decode_chunk<K, F16, REP>(x, lut_bytes, lane4, a_h, a));
     }
   }
 }
@@ -175,7 +183,8 @@ constexpr uint32_t kStagePrefix = 16;
 // CPL: chunks per lane when d == 256 * CPL, 0 for any d (runtime loop).
 // PERM: lookups are visited in the order p.perm (rows still land at their own
 // output position); used to give host-resident tables address locality.
-template <int K, bool SOA, int PF, int CPL, bool PERM>
+// REP: LUT replicas in shared memory (32 or 4).
+template <int K, bool SOA, int PF, int CPL, bool PERM, int REP>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -183,9 +192,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
 
-  // Shared LUT: entry e -> pair e & 511, y1 negated for e >= 512; 32 copies.
-  for (int q = tid; q < kLutEntries * kLutReplicas / 4; q += blockDim.x) {
-    const int e = q >> 3;                               // 8 uint4 per entry
+  // Shared LUT: entry e -> pair e & 511, y1 negated for e >= 512; REP copies.
+  constexpr int kLutBytes = lut_bytes(REP);
+  for (int q = tid; q < kLutEntries * REP / 4; q += blockDim.x) {
+    const int e = q / (REP / 4);                        // REP / 4 uint4 per entry
     uint32_t v = __ldg(p.lut + (e & 511));
     if (e & 512) v ^= 0x80000000u;
     reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
@@ -329,14 +339,168 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
       const uint32_t boff = (kStagePrefix + mis) * 8;
       if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {   // |alpha| in [2^-14, 2^16) or 0
         const __half ah = __float2half_rn(a);             // exact in this range
-        decode_row<K, CPL, true>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
+        decode_row<K, CPL, true, REP>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
       } else {
-        decode_row<K, CPL, false>(w, boff, d, smem, lane, 0, a, orow);
+        decode_row<K, CPL, false, REP>(w, boff, d, smem, lane, 0, a, orow);
       }
     } else {
       for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
     }
     __syncwarp();
+  }
+}
+
+// Host-resident variant for records that fit one 16-byte piece per lane
+// (d <= 1024).  Reads of pinned host memory over the host link are issued as
+// plain 16-byte register loads: asynchronous shared-memory copies of system
+// memory hold their issue queue slots for the whole link round trip and throttle
+// issue.  Each warp keeps PF rows in flight in a register ring (slots fixed at
+// compile time by unrolling) and lands a row into its single shared stage just
+// before decoding it.  16 warps per CTA, so a thread may use up to 128 registers.
+constexpr int kHostWarps = 16;
+
+// 16-byte piece of which only the first `bytes` (even, < 16) are inside the
+// table: 2-byte loads, the rest zero (the table's last record only).
+__device__ __forceinline__ uint4 load_partial16(const uint8_t* src, uint32_t bytes) {
+  uint64_t lo = 0, hi = 0;
+  for (uint32_t b = 0; b < bytes; b += 2) {
+    const uint64_t v = __ldg(reinterpret_cast<const uint16_t*>(src + b));
+    if (b < 8) lo |= v << (8 * b);
+    else hi |= v << (8 * (b - 8));
+  }
+  return make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                    static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
+}
+
+template <int K, bool SOA, int PF, int CPL, int REP>
+__global__ void __launch_bounds__(kHostWarps * 32, 1)
+    lookup_decode_host_kernel(const DecodeParams p) {
+  static_assert(CPL >= 1 && CPL <= 4, "one 16-byte piece per lane");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const uint32_t lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+
+  constexpr int kLutBytes = lut_bytes(REP);
+  for (int q = tid; q < kLutEntries * REP / 4; q += blockDim.x) {
+    const int e = q / (REP / 4);
+    uint32_t v = __ldg(p.lut + (e & 511));
+    if (e & 512) v ^= 0x80000000u;
+    reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
+  }
+  __syncthreads();
+
+  const uint32_t code_bytes = p.code_bytes;
+  const uint32_t d = p.d;
+  const uint64_t n_rows = p.n_rows;
+  const uint64_t stride = p.stride;
+  const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
+  const uintptr_t tbl_end = codes + p.table_bytes;
+  uint8_t* sb = smem + kLutBytes + static_cast<size_t>(warp) * p.stage_bytes + kStagePrefix;
+
+  const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
+  uint64_t n_work = p.n;
+  if (p.n_dev != nullptr) {
+    const uint64_t nd = *p.n_dev;
+    n_work = nd < p.n ? nd : p.n;
+  }
+  const uint64_t lo = gw * n_work / W;
+  const uint64_t hi = (gw + 1) * n_work / W;
+  if (lo >= hi) return;
+  const uint32_t cnt = static_cast<uint32_t>(hi - lo);
+
+  // visiting order: positions j = perm[lo + q] and their ids idx[j], 32 at a time
+  const uint32_t* pos = p.perm + lo;
+  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r) {
+    j = 0;
+    r = 0;
+    if (q < cnt) {
+      j = __ldg(pos + q);
+      r = __ldg(p.idx + j);
+    }
+  };
+  uint32_t jb_cur, jb_nxt;
+  int64_t ib_cur, ib_nxt;
+  load_batch(lane, jb_cur, ib_cur);
+  load_batch(lane + 32, jb_nxt, ib_nxt);
+  uint32_t batch = 0;
+
+  // ring slot of a row: its 16-byte piece, flags | mis << 8, output row, alpha (SoA)
+  uint4 rv[PF];
+  uint32_t rm[PF], rj[PF];
+  uint16_t ra[PF];
+
+  auto issue = [&](uint32_t q, uint4& v, uint32_t& m, uint32_t& jrow, uint16_t& ab) {
+    if (q - batch >= 32) {
+      batch += 32;
+      ib_cur = ib_nxt;
+      jb_cur = jb_nxt;
+      load_batch(batch + 32 + lane, jb_nxt, ib_nxt);
+    }
+    const int64_t r = __shfl_sync(0xffffffffu, ib_cur, static_cast<int>(q - batch));
+    jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
+    m = 0;
+    if (static_cast<uint64_t>(r) < n_rows) {
+      const uintptr_t a = codes + static_cast<uint64_t>(r) * stride;
+      const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
+      const uint32_t mis = static_cast<uint32_t>(a - a0);
+      const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+      if (lane < nch) {
+        const uintptr_t src = a0 + 16u * lane;
+        if (SOA || tbl_end - src >= 16) v = __ldg(reinterpret_cast<const uint4*>(src));
+        else v = load_partial16(reinterpret_cast<const uint8_t*>(src),
+                                static_cast<uint32_t>(tbl_end - src));
+      }
+      if (SOA) ab = __ldg(p.alpha + r);
+      m = 1u | (mis << 8);
+    } else if (lane == 0) {
+      atomicOr(p.status, 1u);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < PF - 1; ++s)
+    if (static_cast<uint32_t>(s) < cnt) issue(s, rv[s], rm[s], rj[s], ra[s]);
+
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (uint32_t g = 0; g < cnt; g += PF) {
+#pragma unroll
+    for (int s = 0; s < PF; ++s) {
+      const uint32_t i = g + s;
+      if (i < cnt) {
+        const int sn = (s + PF - 1) % PF;                // slot of row i + PF - 1
+        if (i + PF - 1 < cnt) issue(i + PF - 1, rv[sn], rm[sn], rj[sn], ra[sn]);
+        const uint32_t m = rm[s];
+        uint4* orow = reinterpret_cast<uint4*>(p.out) + static_cast<uint64_t>(rj[s]) * (d >> 3);
+        if (m & 1u) {
+          const uint32_t mis = m >> 8;
+          const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+          if (lane < nch) *reinterpret_cast<uint4*>(sb + 16u * lane) = rv[s];
+          __syncwarp();
+          uint8_t* code = sb + mis;
+          if (lane == 0)
+            *reinterpret_cast<uint16_t*>(code - 2) =
+                *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+          const uint16_t abits = SOA ? ra[s] : *reinterpret_cast<const uint16_t*>(code + code_bytes);
+          __syncwarp();
+          const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
+          const uint32_t ex = (abits >> 7) & 0xFFu;
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(sb - kStagePrefix);
+          const uint32_t boff = (kStagePrefix + mis) * 8;
+          if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {
+            const __half ah = __float2half_rn(a);
+            decode_row<K, CPL, true, REP>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
+          } else {
+            decode_row<K, CPL, false, REP>(w, boff, d, smem, lane, 0, a, orow);
+          }
+        } else {
+          for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
+        }
+        __syncwarp();
+      }
+    }
   }
 }
 

@@ -45,6 +45,7 @@ struct KernelSet {
 inline bool host_uses_register_ring(int cpl_idx) { return cpl_idx >= 1 && cpl_idx <= 3; }
 constexpr int kPfHostReg = 8;
 
+
 // Host-resident tables: lookups are visited bucketed by row-id range so that
 // consecutive records of a warp are close in the host address space.
 constexpr uint32_t kBucketBits = 12;                  // 4096 ranges

@@ -372,7 +372,7 @@ __device__ __forceinline__ uint4 load_partial16(const uint8_t* src, uint32_t byt
                     static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
 }
 
-template <int K, bool SOA, int PF, int CPL, int REP>
+template <int K, bool SOA, int PF, int CPL, int REP, bool PERM = true>
 __global__ void __launch_bounds__(kHostWarps * 32, 1)
     lookup_decode_host_kernel(const DecodeParams p) {
   static_assert(CPL >= 1 && CPL <= 4, "one 16-byte piece per lane");
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
   const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
   uint64_t n_work = p.n;
-  if (p.n_dev != nullptr) {
+  if (PERM && p.n_dev != nullptr) {
     const uint64_t nd = *p.n_dev;
     n_work = nd < p.n ? nd : p.n;
   }
@@ -411,14 +411,19 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
   if (lo >= hi) return;
   const uint32_t cnt = static_cast<uint32_t>(hi - lo);
 
-  // visiting order: positions j = perm[lo + q] and their ids idx[j], 32 at a time
-  const uint32_t* pos = p.perm + lo;
+  // visiting order: positions j = perm[lo + q] (or lo + q) and their ids, 32 at a time
+  const uint32_t* pos = PERM ? p.perm + lo : nullptr;
   auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r) {
     j = 0;
     r = 0;
     if (q < cnt) {
-      j = __ldg(pos + q);
-      r = __ldg(p.idx + j);
+      if (PERM) {
+        j = __ldg(pos + q);
+        r = __ldg(p.idx + j);
+      } else {
+        j = static_cast<uint32_t>(q);
+        r = __ldg(p.idx + lo + q);
+      }
     }
   };
   uint32_t jb_cur, jb_nxt;
@@ -473,7 +478,8 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
         const int sn = (s + PF - 1) % PF;                // slot of row i + PF - 1
         if (i + PF - 1 < cnt) issue(i + PF - 1, rv[sn], rm[sn], rj[sn], ra[sn]);
         const uint32_t m = rm[s];
-        uint4* orow = reinterpret_cast<uint4*>(p.out) + static_cast<uint64_t>(rj[s]) * (d >> 3);
+        uint4* orow = reinterpret_cast<uint4*>(p.out) +
+                      (PERM ? static_cast<uint64_t>(rj[s]) : lo + i) * (d >> 3);
         if (m & 1u) {
           const uint32_t mis = m >> 8;
           const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;

@@ -143,6 +143,26 @@ cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t 
                                 uint16_t* out, void* stream);
 
 /*
+ * cp_lookup_decode_reduce -- lookup-decode fused with a weighted readout.  The
+ * pages hand the restored rows to "the existing readout" [P4 "how it differs"];
+ * this synthetic readout sums each group of `group` consecutive lookups (for
+ * example the rows one token gathers in one layer), so only one row per group
+ * leaves the kernel:
+ *   out[g][q] = bf16_rn(acc),  acc = fmaf(w[g*group + i], float(row_i[q]), acc)
+ * for i = 0 .. group-1 in order, acc starting at +0 (fp32), where row_i is the
+ * bf16 row cp_lookup_decode would write for idx[g*group + i] (zeros for an
+ * out-of-range id, which also sets the status word) and w = 1 when weights is
+ * NULL.
+ *   idx      device, n_groups * group int64 ids.
+ *   weights  device fp32 [n_groups * group], or NULL.
+ *   out      device bf16 [n_groups][d], 16-byte aligned.
+ * Device-resident tables with d in {256, 512, 1024}; otherwise CP_ERR_INVALID_ARG.
+ */
+cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_t n_groups,
+                                  uint32_t group, const float* weights, uint16_t* out,
+                                  void* stream);
+
+/*
  * cp_get_status -- synchronise `stream`, then report and clear the table's
  * device status word: CP_ERR_INDEX_OOB if any decode since the last call saw an
  * out-of-range id, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK.

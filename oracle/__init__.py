@@ -80,6 +80,10 @@ def lib():
         L.orc_lookup_decode.restype = C.c_uint64
         L.orc_lookup_decode.argtypes = [u8p, C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint64,
                                         u16p, i64p, C.c_uint64, u16p, C.c_int]
+        L.orc_lookup_decode_reduce.restype = C.c_uint64
+        L.orc_lookup_decode_reduce.argtypes = [u8p, C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint64,
+                                               u16p, i64p, C.c_uint64, C.c_uint32,
+                                               C.POINTER(C.c_float), u16p, C.c_int]
         L.orc_distortion.restype = C.c_double
         L.orc_distortion.argtypes = [f64p, u8p, C.c_uint32, C.c_uint32, u16p]
         L.orc_encode_z.restype = C.c_double
@@ -181,6 +185,28 @@ def lookup_decode(records: np.ndarray, n_rows: int, d: int, k: int, rec_bytes: i
     bad = lib().orc_lookup_decode(_p(records, C.c_uint8), n_rows, d, k, rec_bytes,
                                   _p(lut, C.c_uint16), _p(idx, C.c_int64), idx.size,
                                   _p(out, C.c_uint16), n_threads)
+    return out, int(bad)
+
+
+def lookup_decode_reduce(records: np.ndarray, n_rows: int, d: int, k: int, rec_bytes: int,
+                         lut: np.ndarray, idx: np.ndarray, group: int,
+                         weights: np.ndarray | None = None, n_threads: int = 1):
+    """bf16 bits (n_groups, d): per group of `group` lookups, the fp32 fmaf-accumulated
+    weighted sum of the decoded bf16 rows, rounded once to bf16; and the out-of-range count."""
+    records = np.ascontiguousarray(records, dtype=np.uint8)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    assert idx.size % group == 0
+    n_groups = idx.size // group
+    wp = None
+    if weights is not None:
+        weights = np.ascontiguousarray(weights, dtype=np.float32)
+        assert weights.size == idx.size
+        wp = _p(weights, C.c_float)
+    out = np.empty((n_groups, d), dtype=np.uint16)
+    bad = lib().orc_lookup_decode_reduce(_p(records, C.c_uint8), n_rows, d, k, rec_bytes,
+                                         _p(lut, C.c_uint16), _p(idx, C.c_int64), n_groups, group,
+                                         wp, _p(out, C.c_uint16), n_threads)
     return out, int(bad)
 
 

@@ -591,6 +591,34 @@ uint64_t orc_lookup_decode(const uint8_t* records, uint64_t n_rows, uint32_t d, 
   return total;
 }
 
+// Decode fused with a weighted readout (the pages hand the rows to "the
+// existing readout"; this synthetic one sums each group of `group` consecutive
+// lookups): out[g][q] = bf16_rne(acc) with acc = 0 (fp32) and, for i in lookup
+// order, acc = fmaf(w[g*group + i], float(row_i[q]), acc), where row_i is the
+// bf16 row the plain lookup-decode writes (zeros for an out-of-range id) and
+// w = 1 when weights is null.  Returns the count of out-of-range ids.
+uint64_t orc_lookup_decode_reduce(const uint8_t* records, uint64_t n_rows, uint32_t d, uint32_t k,
+                                  uint64_t rec_bytes, const uint16_t* lut, const int64_t* idx,
+                                  uint64_t n_groups, uint32_t group, const float* weights,
+                                  uint16_t* out, int n_threads) {
+  const uint64_t n = n_groups * group;
+  std::vector<uint16_t> rows(n * (uint64_t)d);
+  const uint64_t bad = orc_lookup_decode(records, n_rows, d, k, rec_bytes, lut, idx, n, rows.data(),
+                                         n_threads);
+  for (uint64_t g = 0; g < n_groups; ++g) {
+    for (uint32_t q = 0; q < d; ++q) {
+      float acc = 0.0f;
+      for (uint32_t i = 0; i < group; ++i) {
+        const uint64_t j = g * group + i;
+        const float w = weights ? weights[j] : 1.0f;
+        acc = std::fmaf(w, bf16_to_float(rows[j * d + q]), acc);
+      }
+      out[g * d + q] = float_to_bf16(acc);
+    }
+  }
+  return bad;
+}
+
 // D(c) for a code against a normalised row z.
 double orc_distortion(const double* z, const uint8_t* code, uint32_t d, uint32_t k,
                       const uint16_t* lut) {

@@ -22,6 +22,7 @@ import torch
 __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
+    "lookup_decode_reduce",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -73,6 +74,8 @@ def lib():
         L.cp_last_error.argtypes = []
         L.cp_test_inject_failure.restype = i32
         L.cp_test_inject_failure.argtypes = [i32, i32]
+        L.cp_lookup_decode_reduce.restype = i32
+        L.cp_lookup_decode_reduce.argtypes = [vp, vp, u64, u32, vp, vp, vp]
         L.cp_lookup_decode_host_noalloc.restype = i32
         L.cp_lookup_decode_host_noalloc.argtypes = [vp, u64, u32, u32, vp, vp, u64, vp, vp, vp]
         _lib = L
@@ -176,6 +179,31 @@ def lookup_decode_host(table: Table, idx: torch.Tensor, out: torch.Tensor | None
     """Same as lookup_decode for a table resident in pinned host memory (zero-copy reads)."""
     return _decode(lib().cp_lookup_decode_host, table, idx, out, stream,
                    "cp_lookup_decode_host")
+
+
+def lookup_decode_reduce(table: Table, idx: torch.Tensor, group: int,
+                         weights: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Decode fused with a weighted group readout: bf16 [n // group, d], row g =
+    bf16(sum_i w_i * row_i) over lookups g*group .. g*group+group-1 (fp32 fmaf in order)."""
+    if idx.dtype != torch.int64 or not idx.is_cuda or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int64 CUDA tensor")
+    if group <= 0 or idx.numel() % group:
+        raise ValueError("the number of ids must be a multiple of group")
+    n_groups = idx.numel() // group
+    if out is None:
+        out = torch.empty((n_groups, table.d), dtype=torch.bfloat16, device=idx.device)
+    elif out.dtype != torch.bfloat16 or out.shape != (n_groups, table.d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of shape (n_groups, d)")
+    wp = None
+    if weights is not None:
+        if weights.dtype != torch.float32 or not weights.is_cuda or weights.numel() != idx.numel():
+            raise ValueError("weights must be float32 CUDA with one weight per id")
+        wp = weights.contiguous().data_ptr()
+    _check(lib().cp_lookup_decode_reduce(table.handle, idx.data_ptr(), n_groups, group, wp,
+                                         out.data_ptr(), _stream_ptr(stream)),
+           "cp_lookup_decode_reduce")
+    return out
 
 
 def get_status(table: Table, stream=None) -> int:

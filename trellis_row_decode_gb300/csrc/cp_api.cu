@@ -450,6 +450,69 @@ cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t 
   return decode_common(t, idx, n, out, stream, CP_RESIDENT_HOST);
 }
 
+cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_t n_groups,
+                                  uint32_t group, const float* weights, uint16_t* out,
+                                  void* stream) {
+  if (t == nullptr) return CP_ERR_INVALID_ARG;
+  if (t->residency != CP_RESIDENT_DEVICE) {
+    cpx::set_error("the fused readout needs a device-resident table");
+    return CP_ERR_INVALID_ARG;
+  }
+  if (n_groups == 0) return CP_OK;
+  const int ci = cpk::cpl_index(t->d);
+  if (ci < 1 || ci > 3) {
+    cpx::set_error("the fused readout supports d = 256, 512 or 1024");
+    return CP_ERR_INVALID_ARG;
+  }
+  if (group == 0 || n_groups > kMaxLookups / group || idx == nullptr || out == nullptr ||
+      !aligned(idx, 8) || !aligned(out, 16) || (weights != nullptr && !aligned(weights, 4))) {
+    cpx::set_error("bad ids/weights/output pointer, alignment or counts");
+    return CP_ERR_INVALID_ARG;
+  }
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != t->device) {
+    cpx::set_error("current device differs from the table's device");
+    return CP_ERR_INVALID_ARG;
+  }
+  const bool soa = (t->layout == CP_LAYOUT_SOA);
+  cpk::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = soa ? t->soa_codes : t->rec;
+  p.alpha = soa ? t->soa_alpha : nullptr;
+  p.n_rows = t->n_rows;
+  p.table_bytes = soa ? t->n_rows * t->soa_stride : t->n_rows * t->rec_bytes;
+  p.d = t->d;
+  p.stride = soa ? t->soa_stride : t->rec_bytes;
+  p.code_bytes = t->code_bytes;
+  p.stage_bytes = cpx::stage_bytes(t, soa, &p.alpha_slot);
+  p.lut = t->lut_dev;
+  p.idx = idx;
+  p.n = n_groups * group;
+  p.out = out;
+  p.status = t->status_dev;
+  const int nwarps = cpk::kReduceWarps;
+  const size_t smem = static_cast<size_t>(cpk::lut_bytes(32)) +
+                      static_cast<size_t>(nwarps) * cpk::kPfReduce * (p.stage_bytes + 8);
+  if (smem > static_cast<size_t>(t->max_smem)) return CP_ERR_INVALID_ARG;
+  cpk::ReduceFn fn = t->kernels.reduce[soa ? 1 : 0][ci - 1];
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  uint64_t blocks = (n_groups + nwarps - 1) / nwarps;
+  if (blocks > static_cast<uint64_t>(t->sm_count)) blocks = t->sm_count;
+  if ((n_groups / (blocks * nwarps) + 1) * group >= (1ull << 31)) {
+    cpx::set_error("too many lookups for one launch");
+    return CP_ERR_INVALID_ARG;
+  }
+  void* args[] = {&p, &weights, &group, &n_groups};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
+                       dim3(nwarps * 32), args, smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fused readout launch");
+  return CP_OK;
+}
+
 cp_status cp_get_status(const cp_table* t, void* stream) {
   if (t == nullptr) return CP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

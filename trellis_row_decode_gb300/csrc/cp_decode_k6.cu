@@ -28,6 +28,12 @@ KernelSet kernels_k6() {
   s.host[1][1] = &lookup_decode_host_kernel<6, true, kPfHostReg, 1, 32>;
   s.host[1][2] = &lookup_decode_host_kernel<6, true, kPfHostReg, 2, 32>;
   s.host[1][3] = &lookup_decode_host_kernel<6, true, kPfHostReg, 4, 32>;
+  s.reduce[0][0] = &lookup_decode_reduce_kernel<6, false, kPfReduce, 1>;
+  s.reduce[0][1] = &lookup_decode_reduce_kernel<6, false, kPfReduce, 2>;
+  s.reduce[0][2] = &lookup_decode_reduce_kernel<6, false, kPfReduce, 4>;
+  s.reduce[1][0] = &lookup_decode_reduce_kernel<6, true, kPfReduce, 1>;
+  s.reduce[1][1] = &lookup_decode_reduce_kernel<6, true, kPfReduce, 2>;
+  s.reduce[1][2] = &lookup_decode_reduce_kernel<6, true, kPfReduce, 4>;
   return s;
 }
 

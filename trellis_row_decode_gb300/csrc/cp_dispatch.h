@@ -2,26 +2,24 @@
 #pragma once
 
 #include "cp_kernels.cuh"
+#include "cp_kernels_host.cuh"
+#include "cp_kernels_reduce.cuh"
 
 namespace cpk {
 
 // Stages of the per-warp record ring: one row ahead for HBM-resident tables,
 // more rows in flight for tables read over the host link (higher latency).
-#ifndef CP_PF_DEVICE
-#define CP_PF_DEVICE 2
-#endif
 #ifndef CP_PF_HOST
 #define CP_PF_HOST 16
 #endif
 #ifndef CP_LUTREP_HOST
 #define CP_LUTREP_HOST 4
 #endif
-constexpr int kPfDevice = CP_PF_DEVICE;
 constexpr int kPfHost = CP_PF_HOST;
-constexpr int kLutRepDevice = 32;
 constexpr int kLutRepHost = CP_LUTREP_HOST;
 
 using DecodeFn = void (*)(DecodeParams);
+using ReduceFn = void (*)(DecodeParams, const float*, uint32_t, uint64_t);
 
 // Chunks-per-lane specialisations: index 0 = any d (runtime loop), index i > 0
 // = d == 256 * kCplValues[i].
@@ -38,7 +36,12 @@ struct KernelSet {
   DecodeFn dev[2][kCplVariants];    // [layout AoS/SoA][cpl index], lookup order
   DecodeFn host[2][kCplVariants];   // bucketed order: register-ring kernel for cpl
                                     // indices 1..3 (d <= 1024), cp.async kernel otherwise
+  ReduceFn reduce[2][3];            // decode + group readout, d = 256, 512, 1024
 };
+#ifndef CP_PF_REDUCE
+#define CP_PF_REDUCE 2
+#endif
+constexpr int kPfReduce = CP_PF_REDUCE;
 
 // Host-path kernels for cpl indices 1..3 are lookup_decode_host_kernel (one
 // shared stage per warp, kHostWarps warps per CTA).

@@ -61,6 +61,7 @@ HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb);
 void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb);
 
 bool geometry_ok(uint32_t d, uint32_t k);
+uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot);
 uint32_t soa_stride(uint32_t d, uint32_t k);
 bool aligned(const void* p, uintptr_t a);
 cpk::KernelSet kernels_for(uint32_t k);

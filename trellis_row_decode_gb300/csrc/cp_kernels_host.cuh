@@ -1,0 +1,168 @@
+// cp_kernels_host.cuh -- host-resident lookup-decode kernel (register ring).
+#pragma once
+
+#include "cp_kernels.cuh"
+
+namespace cpk {
+
+// Host-resident variant for records that fit one 16-byte piece per lane
+// (d <= 1024).  Reads of pinned host memory over the host link are issued as
+// plain 16-byte register loads: asynchronous shared-memory copies of system
+// memory hold their issue queue slots for the whole link round trip and throttle
+// issue.  Each warp keeps PF rows in flight in a register ring (slots fixed at
+// compile time by unrolling) and lands a row into its single shared stage just
+// before decoding it.  16 warps per CTA, so a thread may use up to 128 registers.
+constexpr int kHostWarps = 16;
+
+// 16-byte piece of which only the first `bytes` (even, < 16) are inside the
+// table: 2-byte loads, the rest zero (the table's last record only).
+__device__ __forceinline__ uint4 load_partial16(const uint8_t* src, uint32_t bytes) {
+  uint64_t lo = 0, hi = 0;
+  for (uint32_t b = 0; b < bytes; b += 2) {
+    const uint64_t v = __ldg(reinterpret_cast<const uint16_t*>(src + b));
+    if (b < 8) lo |= v << (8 * b);
+    else hi |= v << (8 * (b - 8));
+  }
+  return make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                    static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
+}
+
+template <int K, bool SOA, int PF, int CPL, int REP, bool PERM = true>
+__global__ void __launch_bounds__(kHostWarps * 32, 1)
+    lookup_decode_host_kernel(const DecodeParams p) {
+  static_assert(CPL >= 1 && CPL <= 4, "one 16-byte piece per lane");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const uint32_t lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+
+  constexpr int kLutBytes = lut_bytes(REP);
+  for (int q = tid; q < kLutEntries * REP / 4; q += blockDim.x) {
+    const int e = q / (REP / 4);
+    uint32_t v = __ldg(p.lut + (e & 511));
+    if (e & 512) v ^= 0x80000000u;
+    reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
+  }
+  __syncthreads();
+
+  const uint32_t code_bytes = p.code_bytes;
+  const uint32_t d = p.d;
+  const uint64_t n_rows = p.n_rows;
+  const uint64_t stride = p.stride;
+  const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
+  const uintptr_t tbl_end = codes + p.table_bytes;
+  uint8_t* sb = smem + kLutBytes + static_cast<size_t>(warp) * p.stage_bytes + kStagePrefix;
+
+  const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
+  uint64_t n_work = p.n;
+  if (PERM && p.n_dev != nullptr) {
+    const uint64_t nd = *p.n_dev;
+    n_work = nd < p.n ? nd : p.n;
+  }
+  const uint64_t lo = gw * n_work / W;
+  const uint64_t hi = (gw + 1) * n_work / W;
+  if (lo >= hi) return;
+  const uint32_t cnt = static_cast<uint32_t>(hi - lo);
+
+  // visiting order: positions j = perm[lo + q] (or lo + q) and their ids, 32 at a time
+  const uint32_t* pos = PERM ? p.perm + lo : nullptr;
+  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r) {
+    j = 0;
+    r = 0;
+    if (q < cnt) {
+      if (PERM) {
+        j = __ldg(pos + q);
+        r = __ldg(p.idx + j);
+      } else {
+        j = static_cast<uint32_t>(q);
+        r = __ldg(p.idx + lo + q);
+      }
+    }
+  };
+  uint32_t jb_cur, jb_nxt;
+  int64_t ib_cur, ib_nxt;
+  load_batch(lane, jb_cur, ib_cur);
+  load_batch(lane + 32, jb_nxt, ib_nxt);
+  uint32_t batch = 0;
+
+  // ring slot of a row: its 16-byte piece, flags | mis << 8, output row, alpha (SoA)
+  uint4 rv[PF];
+  uint32_t rm[PF], rj[PF];
+  uint16_t ra[PF];
+
+  auto issue = [&](uint32_t q, uint4& v, uint32_t& m, uint32_t& jrow, uint16_t& ab) {
+    if (q - batch >= 32) {
+      batch += 32;
+      ib_cur = ib_nxt;
+      jb_cur = jb_nxt;
+      load_batch(batch + 32 + lane, jb_nxt, ib_nxt);
+    }
+    const int64_t r = __shfl_sync(0xffffffffu, ib_cur, static_cast<int>(q - batch));
+    jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
+    m = 0;
+    if (static_cast<uint64_t>(r) < n_rows) {
+      const uintptr_t a = codes + static_cast<uint64_t>(r) * stride;
+      const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
+      const uint32_t mis = static_cast<uint32_t>(a - a0);
+      const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+      if (lane < nch) {
+        const uintptr_t src = a0 + 16u * lane;
+        if (SOA || tbl_end - src >= 16) v = __ldg(reinterpret_cast<const uint4*>(src));
+        else v = load_partial16(reinterpret_cast<const uint8_t*>(src),
+                                static_cast<uint32_t>(tbl_end - src));
+      }
+      if (SOA) ab = __ldg(p.alpha + r);
+      m = 1u | (mis << 8);
+    } else if (lane == 0) {
+      atomicOr(p.status, 1u);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < PF - 1; ++s)
+    if (static_cast<uint32_t>(s) < cnt) issue(s, rv[s], rm[s], rj[s], ra[s]);
+
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (uint32_t g = 0; g < cnt; g += PF) {
+#pragma unroll
+    for (int s = 0; s < PF; ++s) {
+      const uint32_t i = g + s;
+      if (i < cnt) {
+        const int sn = (s + PF - 1) % PF;                // slot of row i + PF - 1
+        if (i + PF - 1 < cnt) issue(i + PF - 1, rv[sn], rm[sn], rj[sn], ra[sn]);
+        const uint32_t m = rm[s];
+        uint4* orow = reinterpret_cast<uint4*>(p.out) +
+                      (PERM ? static_cast<uint64_t>(rj[s]) : lo + i) * (d >> 3);
+        if (m & 1u) {
+          const uint32_t mis = m >> 8;
+          const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+          if (lane < nch) *reinterpret_cast<uint4*>(sb + 16u * lane) = rv[s];
+          __syncwarp();
+          uint8_t* code = sb + mis;
+          if (lane == 0)
+            *reinterpret_cast<uint16_t*>(code - 2) =
+                *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+          const uint16_t abits = SOA ? ra[s] : *reinterpret_cast<const uint16_t*>(code + code_bytes);
+          __syncwarp();
+          const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
+          const uint32_t ex = (abits >> 7) & 0xFFu;
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(sb - kStagePrefix);
+          const uint32_t boff = (kStagePrefix + mis) * 8;
+          if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {
+            const __half ah = __float2half_rn(a);
+            decode_row<K, CPL, true, REP>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
+          } else {
+            decode_row<K, CPL, false, REP>(w, boff, d, smem, lane, 0, a, orow);
+          }
+        } else {
+          for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
+        }
+        __syncwarp();
+      }
+    }
+  }
+}
+
+}  // namespace cpk

@@ -143,6 +143,27 @@ cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t 
                                 uint16_t* out, void* stream);
 
 /*
+ * cp_table_set_cache -- frequency-based caching for a host-resident table: keep
+ * device copies of the records of `m` hot rows, so that cp_lookup_decode_host
+ * reads them from HBM instead of over the host link.  The pages name access
+ * counts as the input of frequency-based caching [P1 "Perspective"; P4
+ * "assumptions and limits"]; the caller chooses the rows (e.g. the most
+ * frequent ids of past traffic).
+ *   hot_rows  host pointer, m distinct ids in [0, n_rows) (any order).
+ *   cache     device buffer of m * R bytes, 16-byte aligned, owned by the caller;
+ *             it receives the records (AoS, ascending row order).
+ *   m = 0     removes the cache.  Replacing a cache synchronises `stream` first.
+ * The call allocates the cache map (2^ceil(log2(2m)) slots of 12 bytes plus
+ * 8m bytes, owned by the handle) and returns after the cache is built (it
+ * synchronises `stream`).  Output of cp_lookup_decode_host is unchanged, bit for
+ * bit.  Host-resident AoS tables with d = 256, 512 or 1024; otherwise
+ * CP_ERR_INVALID_ARG.  Not to be called while decodes on the handle are in
+ * flight on other streams.
+ */
+cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, void* cache,
+                             void* stream);
+
+/*
  * cp_lookup_decode_reduce -- lookup-decode fused with a weighted readout.  The
  * pages hand the restored rows to "the existing readout" [P4 "how it differs"];
  * this synthetic readout sums each group of `group` consecutive lookups (for

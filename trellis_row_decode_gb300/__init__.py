@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
-    "lookup_decode_reduce",
+    "lookup_decode_reduce", "set_cache",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -74,6 +74,8 @@ def lib():
         L.cp_last_error.argtypes = []
         L.cp_test_inject_failure.restype = i32
         L.cp_test_inject_failure.argtypes = [i32, i32]
+        L.cp_table_set_cache.restype = i32
+        L.cp_table_set_cache.argtypes = [vp, vp, u64, vp, vp]
         L.cp_lookup_decode_reduce.restype = i32
         L.cp_lookup_decode_reduce.argtypes = [vp, vp, u64, u32, vp, vp, vp]
         L.cp_lookup_decode_host_noalloc.restype = i32
@@ -204,6 +206,20 @@ def lookup_decode_reduce(table: Table, idx: torch.Tensor, group: int,
                                          out.data_ptr(), _stream_ptr(stream)),
            "cp_lookup_decode_reduce")
     return out
+
+
+def set_cache(table: Table, hot_rows, cache: torch.Tensor | None = None, stream=None) -> None:
+    """Keep device copies of the records of `hot_rows` (distinct ids) for a host-resident
+    table; `cache` is a uint8 CUDA tensor of len(hot_rows) * R bytes (allocated if None).
+    An empty list removes the cache."""
+    rows = np.ascontiguousarray(np.asarray(hot_rows, dtype=np.int64))
+    m = rows.size
+    if m and cache is None:
+        cache = torch.empty(m * record_bytes(table.d, table.k), dtype=torch.uint8, device="cuda")
+    ptr = cache.data_ptr() if m else None
+    _check(lib().cp_table_set_cache(table.handle, rows.ctypes.data if m else None, m, ptr,
+                                    _stream_ptr(stream)), "cp_table_set_cache")
+    table._cache = cache if m else None
 
 
 def get_status(table: Table, stream=None) -> int:

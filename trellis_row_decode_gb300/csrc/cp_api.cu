@@ -1,11 +1,13 @@
 // cp_api.cu -- host side of libcp: validation, table handles, launches.
 // The operations are specified in include/cp.h.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -46,6 +48,7 @@ HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb) {
   h.dup = h.owner + 2ull * capacity;
   h.counts = h.dup + capacity;
   h.perm = h.counts + ((nb + 1 + 63) & ~63u);
+  h.cslot = h.perm + capacity;
   return h;
 }
 
@@ -166,13 +169,21 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     if (e == cudaSuccess)
       e = cudaMemsetAsync(counts, 0, (t->bucket_nb + 1) * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "scratch reset");
-    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, t->sm_count, stream);
+    const bool cached = t->cache != nullptr && t->cmap_ts != 0;
+    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, cached ? t->cmap_keys : nullptr,
+                       cached ? t->cmap_vals : nullptr, cached ? t->cmap_ts : 0,
+                       cached ? hs->cslot : nullptr, t->sm_count, stream);
     cpk::launch_bucket_partition(idx + c0, dup, m, t->n_rows, t->bucket_shift, t->bucket_nb,
                                  counts, perm, t->sm_count, stream);
     cpk::DecodeParams pc = p;
     pc.idx = idx + c0;
     pc.perm = perm;
     pc.n_dev = counts + t->bucket_nb;                   // visits = owners + out-of-range ids
+    if (cached) {
+      pc.cslot = hs->cslot;
+      pc.cache = t->cache;
+      pc.cache_bytes = t->cache_rows * t->rec_bytes;
+    }
     pc.n = m;
     pc.out = out + c0 * t->d;
     uint64_t bl = (m + nwarps - 1) / nwarps;
@@ -291,6 +302,7 @@ void cp_table_free(cp_table* t) {
   if (t->lut_dev) cudaFree(t->lut_dev);
   if (t->status_dev) cudaFree(t->status_dev);
   if (t->scratch_dev) cudaFree(t->scratch_dev);
+  if (t->cmap_keys) cudaFree(t->cmap_keys);
   if (t->registered) cudaHostUnregister(t->registered);
   if (prev >= 0 && prev != t->device) cudaSetDevice(prev);
   delete t;
@@ -448,6 +460,83 @@ cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, ui
 cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t n,
                                 uint16_t* out, void* stream) {
   return decode_common(t, idx, n, out, stream, CP_RESIDENT_HOST);
+}
+
+cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, void* cache,
+                             void* stream) {
+  if (t == nullptr) return CP_ERR_INVALID_ARG;
+  if (t->residency != CP_RESIDENT_HOST || t->layout != CP_LAYOUT_AOS ||
+      !cpk::host_uses_register_ring(cpk::cpl_index(t->d))) {
+    cpx::set_error("the hot-row cache applies to host-resident AoS tables with d = 256, 512 or 1024");
+    return CP_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (t->cmap_keys != nullptr) {            // drop the previous cache (after pending work)
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    cudaFree(t->cmap_keys);
+    t->cmap_keys = nullptr;
+    t->cmap_vals = nullptr;
+    t->cmap_ts = 0;
+    t->cache = nullptr;
+    t->cache_rows = 0;
+  }
+  if (m == 0) return CP_OK;
+  if (hot_rows == nullptr || cache == nullptr || !aligned(cache, 16) || m > (1ull << 30) ||
+      m > t->n_rows) {
+    cpx::set_error("bad hot-row list, cache pointer/alignment or count");
+    return CP_ERR_INVALID_ARG;
+  }
+  std::vector<int64_t> rows(hot_rows, hot_rows + m);
+  std::sort(rows.begin(), rows.end());            // ascending: link-friendly copy order
+  for (uint64_t i = 0; i < m; ++i) {
+    if (rows[i] < 0 || static_cast<uint64_t>(rows[i]) >= t->n_rows || (i > 0 && rows[i] == rows[i - 1])) {
+      cpx::set_error("hot rows must be distinct ids in [0, n_rows)");
+      return CP_ERR_INVALID_ARG;
+    }
+  }
+  uint32_t ts = 1024;
+  while (ts < 2 * m) ts <<= 1;
+  if (take_injected(g_fail_alloc)) {
+    cpx::set_error("injected device allocation failure");
+    return CP_ERR_NO_MEMORY;
+  }
+  void* mem = nullptr;
+  const size_t bytes = static_cast<size_t>(ts) * (sizeof(unsigned long long) + sizeof(uint32_t)) +
+                       m * sizeof(int64_t);
+  cudaError_t e = cudaMalloc(&mem, bytes);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaMalloc(cache map)");
+    return CP_ERR_NO_MEMORY;
+  }
+  unsigned long long* keys = static_cast<unsigned long long*>(mem);
+  uint32_t* vals = reinterpret_cast<uint32_t*>(keys + ts);
+  int64_t* rows_dev = reinterpret_cast<int64_t*>(vals + ts);
+  e = cudaMemsetAsync(keys, 0, ts * sizeof(unsigned long long), s);
+  if (e == cudaSuccess)   // pageable source: returns once the data is staged
+    e = cudaMemcpyAsync(rows_dev, rows.data(), m * sizeof(int64_t), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    cudaFree(mem);
+    return cuda_fail(e, "cache map upload");
+  }
+  cpk::launch_cache_build(t->rec, t->rec_bytes, rows_dev, m, static_cast<uint8_t*>(cache), keys, vals,
+                          ts, t->sm_count, s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFree(mem);
+    return cuda_fail(e, "cache build launch");
+  }
+  e = cudaStreamSynchronize(s);                  // rows_dev must stay valid until then
+  if (e != cudaSuccess) {
+    cudaFree(mem);
+    return cuda_fail(e, "cache build");
+  }
+  t->cmap_keys = keys;
+  t->cmap_vals = vals;
+  t->cmap_ts = ts;
+  t->cache = static_cast<const uint8_t*>(cache);
+  t->cache_rows = m;
+  return CP_OK;
 }
 
 cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_t n_groups,

@@ -44,9 +44,18 @@ __device__ __forceinline__ bool visits(const uint32_t* dup, uint64_t j) {
 // probe (the group's lowest lane probes); slots are read before any CAS, so the
 // lookups of a hot id do not serialise on one atomic.  Probing is bounded by ts;
 // a lookup that finds no slot owns itself (still correct, just not deduplicated).
+__device__ __forceinline__ uint32_t slot_hash(unsigned long long key, uint32_t ts) {
+  return static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
+}
+
+// With a hot-row cache (cmap_ts > 0) the group's lowest lane also looks the id
+// up in the cache map (keys r + 1 -> slot) and the group writes cslot[j].
 __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint64_t n_rows,
                               unsigned long long* __restrict__ keys, uint32_t* __restrict__ owner,
-                              uint32_t ts, uint32_t* __restrict__ dup) {
+                              uint32_t ts, uint32_t* __restrict__ dup,
+                              const unsigned long long* __restrict__ cmap_keys,
+                              const uint32_t* __restrict__ cmap_vals, uint32_t cmap_ts,
+                              uint32_t* __restrict__ cslot) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
@@ -54,15 +63,31 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
     const uint64_t j = base + lane;
     const int64_t r = (j < n) ? __ldg(idx + j) : -1;
     const bool valid = j < n && static_cast<uint64_t>(r) < n_rows;
-    if (j < n && !valid) dup[j] = kNoOwner;
+    if (j < n && !valid) {
+      dup[j] = kNoOwner;
+      if (cmap_ts != 0) cslot[j] = kNoOwner;
+    }
     const uint32_t active = __ballot_sync(0xffffffffu, valid);
     if (!valid) continue;
     const unsigned long long key = static_cast<unsigned long long>(r) + 1ull;
     const uint32_t group = __match_any_sync(active, key);
     const uint32_t leader = __ffs(group) - 1;
     uint32_t o = static_cast<uint32_t>(j);
+    uint32_t cs = kNoOwner;
+    if (lane == leader && cmap_ts != 0) {
+      uint32_t slot = slot_hash(key, cmap_ts);
+      for (uint32_t probe = 0; probe < cmap_ts; ++probe) {
+        const unsigned long long kk = __ldg(cmap_keys + slot);
+        if (kk == key) {
+          cs = __ldg(cmap_vals + slot);
+          break;
+        }
+        if (kk == 0ull) break;
+        slot = (slot + 1) & (cmap_ts - 1);
+      }
+    }
     if (lane == leader) {
-      uint32_t slot = static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
+      uint32_t slot = slot_hash(key, ts);
       for (uint32_t probe = 0; probe < ts; ++probe) {
         unsigned long long cur = __ldcg(keys + slot);
         if (cur == 0ull) {
@@ -83,6 +108,40 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
     }
     o = __shfl_sync(group, o, leader);
     dup[j] = o;
+    if (cmap_ts != 0) cslot[j] = __shfl_sync(group, cs, leader);
+  }
+}
+
+// Cache construction: warp per hot row, 2-byte granules (records are 2-byte
+// aligned); then one thread per row inserts row + 1 -> slot.
+__global__ void cache_fill_kernel(const uint8_t* __restrict__ table, uint32_t R,
+                                  const int64_t* __restrict__ rows, uint64_t m,
+                                  uint8_t* __restrict__ cache) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t s = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       s < m; s += warps) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(table + static_cast<uint64_t>(rows[s]) * R);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(cache + s * R);
+    for (uint32_t i = lane; i < R / 2; i += 32) dst[i] = src[i];
+  }
+}
+
+__global__ void cache_map_kernel(const int64_t* __restrict__ rows, uint64_t m,
+                                 unsigned long long* __restrict__ keys,
+                                 uint32_t* __restrict__ vals, uint32_t ts) {
+  const uint64_t T = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t s = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; s < m; s += T) {
+    const unsigned long long key = static_cast<unsigned long long>(rows[s]) + 1ull;
+    uint32_t slot = slot_hash(key, ts);
+    for (uint32_t probe = 0; probe < ts; ++probe) {
+      const unsigned long long prev = atomicCAS(keys + slot, 0ull, key);
+      if (prev == 0ull) {
+        vals[slot] = static_cast<uint32_t>(s);
+        break;
+      }
+      slot = (slot + 1) & (ts - 1);
+    }
   }
 }
 
@@ -177,9 +236,18 @@ __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, const uin
 }  // namespace
 
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
-                   uint32_t* owner, uint32_t ts, uint32_t* dup, int sm_count, cudaStream_t s) {
-  dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(idx, n, n_rows, keys, owner, ts,
-                                                                     dup);  // warp-strided
+                   uint32_t* owner, uint32_t ts, uint32_t* dup,
+                   const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
+                   uint32_t cmap_ts, uint32_t* cslot, int sm_count, cudaStream_t s) {
+  dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(
+      idx, n, n_rows, keys, owner, ts, dup, cmap_keys, cmap_vals, cmap_ts, cslot);
+}
+
+void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, uint64_t m,
+                        uint8_t* cache, unsigned long long* keys, uint32_t* vals, uint32_t ts,
+                        int sm_count, cudaStream_t s) {
+  cache_fill_kernel<<<static_cast<unsigned>(sm_count) * 4, 512, 0, s>>>(table, R, rows, m, cache);
+  cache_map_kernel<<<static_cast<unsigned>(sm_count) * 4, 256, 0, s>>>(rows, m, keys, vals, ts);
 }
 
 void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,

@@ -58,8 +58,19 @@ constexpr uint32_t kHashSlotsMax = 2 * kBucketChunk;  // dedupe table slots (loa
 // dup[j] = owner lookup of idx[j] among n lookups (kNoOwner for ids outside
 // [0, n_rows)); keys (ts 64-bit words, zeroed) and owner (ts words, 0xFF-filled)
 // are the open-addressing table, ts a power of two >= 2n.
+// With a hot-row cache map (cmap_ts > 0), also cslot[j] = cache slot of idx[j]
+// (or 0xFFFFFFFF when the id is not cached).
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
-                   uint32_t* owner, uint32_t ts, uint32_t* dup, int sm_count, cudaStream_t s);
+                   uint32_t* owner, uint32_t ts, uint32_t* dup,
+                   const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
+                   uint32_t cmap_ts, uint32_t* cslot, int sm_count, cudaStream_t s);
+
+// Hot-row cache construction: records of the m rows `rows` (device ids, sorted)
+// copied from the host table alias into `cache` (stride R), and the map
+// row + 1 -> slot inserted into keys/vals (ts slots, keys zeroed by the caller).
+void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, uint64_t m,
+                        uint8_t* cache, unsigned long long* keys, uint32_t* vals, uint32_t ts,
+                        int sm_count, cudaStream_t s);
 
 // Partition of the lookups that own their id (all of them if dup is null) by
 // (id >> shift), ids outside [0, n_rows) in the last bucket.  counts: nb + 1

@@ -25,6 +25,11 @@ struct cp_table {
   uint32_t* lut_dev;      // 512 words
   uint32_t* status_dev;   // 1 word
   void* scratch_dev;      // host-resident tables: see cpx::HostScratch (kBucketChunk capacity)
+  const uint8_t* cache;   // host-resident tables: device copies of hot records (cache_rows x R)
+  uint64_t cache_rows;
+  unsigned long long* cmap_keys;   // row id + 1 -> cache slot, open addressing (cmap_ts slots)
+  uint32_t* cmap_vals;
+  uint32_t cmap_ts;
   uint32_t bucket_shift;  // bucket of row r = r >> bucket_shift
   uint32_t bucket_nb;     // number of row-range buckets
   void* registered;       // host range this handle registered, else nullptr
@@ -47,12 +52,13 @@ struct HostScratch {
   uint32_t* dup;
   uint32_t* counts;
   uint32_t* perm;
+  uint32_t* cslot;        // cache slot of each lookup's id (hot-row cache), else ~0
   uint32_t capacity;
 };
 
 constexpr size_t host_scratch_bytes(uint32_t capacity, uint32_t nb) {
   return static_cast<size_t>(2) * capacity * (sizeof(unsigned long long) + sizeof(uint32_t)) +
-         (static_cast<size_t>(2) * capacity + ((nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
+         (static_cast<size_t>(3) * capacity + ((nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
 }
 
 HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb);

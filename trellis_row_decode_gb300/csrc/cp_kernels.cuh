@@ -70,6 +70,9 @@ struct DecodeParams {
   const int64_t* idx;
   const uint32_t* perm;     // processing order (PERM kernels): position i decodes lookup perm[i]
   const uint32_t* n_dev;    // PERM kernels: number of positions, read on the device
+  const uint32_t* cslot;    // host path: cache slot per lookup (0xFFFFFFFF: not cached) or null
+  const uint8_t* cache;     // host path: device copies of hot records, stride = record bytes
+  uint64_t cache_bytes;
   uint64_t n;
   uint16_t* out;            // bf16 [n][d], 16-byte aligned
   uint32_t* status;         // bit 0: an id was out of range

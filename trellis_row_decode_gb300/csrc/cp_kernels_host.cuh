@@ -66,25 +66,31 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
   if (lo >= hi) return;
   const uint32_t cnt = static_cast<uint32_t>(hi - lo);
 
-  // visiting order: positions j = perm[lo + q] (or lo + q) and their ids, 32 at a time
+  // visiting order: positions j = perm[lo + q] (or lo + q), their ids and, with a
+  // hot-row cache, their cache slots, 32 at a time
   const uint32_t* pos = PERM ? p.perm + lo : nullptr;
-  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r) {
+  const uint32_t* cslot = PERM ? p.cslot : nullptr;
+  const uintptr_t cache = reinterpret_cast<uintptr_t>(p.cache);
+  const uintptr_t cache_end = cache + p.cache_bytes;
+  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r, uint32_t& c) {
     j = 0;
     r = 0;
+    c = 0xFFFFFFFFu;
     if (q < cnt) {
       if (PERM) {
         j = __ldg(pos + q);
         r = __ldg(p.idx + j);
+        if (cslot != nullptr) c = __ldg(cslot + j);
       } else {
         j = static_cast<uint32_t>(q);
         r = __ldg(p.idx + lo + q);
       }
     }
   };
-  uint32_t jb_cur, jb_nxt;
+  uint32_t jb_cur, jb_nxt, cb_cur, cb_nxt;
   int64_t ib_cur, ib_nxt;
-  load_batch(lane, jb_cur, ib_cur);
-  load_batch(lane + 32, jb_nxt, ib_nxt);
+  load_batch(lane, jb_cur, ib_cur, cb_cur);
+  load_batch(lane + 32, jb_nxt, ib_nxt, cb_nxt);
   uint32_t batch = 0;
 
   // ring slot of a row: its 16-byte piece, flags | mis << 8, output row, alpha (SoA)
@@ -97,21 +103,27 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
       batch += 32;
       ib_cur = ib_nxt;
       jb_cur = jb_nxt;
-      load_batch(batch + 32 + lane, jb_nxt, ib_nxt);
+      cb_cur = cb_nxt;
+      load_batch(batch + 32 + lane, jb_nxt, ib_nxt, cb_nxt);
     }
     const int64_t r = __shfl_sync(0xffffffffu, ib_cur, static_cast<int>(q - batch));
     jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
+    const uint32_t cs = __shfl_sync(0xffffffffu, cb_cur, static_cast<int>(q - batch));
     m = 0;
     if (static_cast<uint64_t>(r) < n_rows) {
-      const uintptr_t a = codes + static_cast<uint64_t>(r) * stride;
+      // a cached id reads its AoS record from HBM (cache slots are AoS, stride R)
+      const bool hot = !SOA && cs != 0xFFFFFFFFu;
+      const uintptr_t a = hot ? cache + static_cast<uint64_t>(cs) * stride
+                              : codes + static_cast<uint64_t>(r) * stride;
+      const uintptr_t end = hot ? cache_end : tbl_end;
       const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
       const uint32_t mis = static_cast<uint32_t>(a - a0);
       const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
       if (lane < nch) {
         const uintptr_t src = a0 + 16u * lane;
-        if (SOA || tbl_end - src >= 16) v = __ldg(reinterpret_cast<const uint4*>(src));
+        if (SOA || end - src >= 16) v = __ldg(reinterpret_cast<const uint4*>(src));
         else v = load_partial16(reinterpret_cast<const uint8_t*>(src),
-                                static_cast<uint32_t>(tbl_end - src));
+                                static_cast<uint32_t>(end - src));
       }
       if (SOA) ab = __ldg(p.alpha + r);
       m = 1u | (mis << 8);

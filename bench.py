@@ -336,6 +336,31 @@ def our_arm(args, w, rank, world, local):
                  "frac_of_hbm_peak": fbytes / tm / 1e9 / measured_peaks()[0]}
         del red_out, gates
 
+    # Mixed per-row bit rates (frequency-based allocation): 2^24 rows x the same d,
+    # rates uniform over b = 1.5 .. 3, the same replay shape.
+    mixed = None
+    if w.d % 32 == 0 and w.d <= 4096 and rank == 0:
+        mrows = 1 << 24
+        ks = synth.mixed_rates(synth.SEED_TABLE, torch.arange(mrows, device="cuda"))
+        moffs = synth.mixed_offsets(ks, w.d)
+        mbuf = torch.empty(int(moffs[-1].item()), dtype=torch.uint8, device="cuda")
+        synth.fill_mixed_records(mbuf, synth.SEED_TABLE, ks, moffs, w.d)
+        mtable = cp.load_mixed_table(mbuf, moffs, w.d)
+        midx = torch.from_numpy(synth.zipf_indices(synth.SEED_INDEX, n, mrows)).cuda()
+        mrec = (moffs[1:] - moffs[:-1])[midx].sum().item()
+        tmx = time_steps(lambda: cp.lookup_decode(mtable, midx, out, stream), min(args.steps, 500),
+                         args.warmup, flush, stream)
+        assert cp.get_status(mtable) == cp.CP_OK
+        tmm = float(np.median(tmx))
+        mbytes = mrec + n * (2 * w.d + 8 + 16)
+        mixed = {"entry_point": "cp_lookup_decode (mixed-rate table)", "n_rows": mrows,
+                 "mean_bits_per_param": float(mbuf.numel() * 8 / (mrows * w.d)),
+                 "ms_per_step": tmm * 1e3, "rows_per_s": n / tmm,
+                 "algorithmic_gbs": mbytes / tmm / 1e9,
+                 "frac_of_hbm_peak": mbytes / tmm / 1e9 / measured_peaks()[0]}
+        mtable.close()
+        del mbuf, moffs, ks, midx
+
     # End to end through the public API: ids from pinned host memory, rows back
     # to pinned host memory, both copies inside the timed region.
     idx_h = torch.from_numpy(idx_np).pin_memory()
@@ -399,6 +424,8 @@ def our_arm(args, w, rank, world, local):
             line["host_path"] = host_obj
         if fused is not None:
             line["fused_readout"] = fused
+        if mixed is not None:
+            line["mixed_rate"] = mixed
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

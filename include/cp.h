@@ -113,6 +113,23 @@ cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, ui
                         int layout, void* soa_dst, void* stream);
 
 /*
+ * cp_table_load_mixed -- bind a table whose rows have different code rates
+ * (frequency-based bit allocation, tried on [P4 "assumptions and limits"]):
+ * record r, [code at k_r bits per step][bf16 alpha], occupies bytes
+ * [offsets[r], offsets[r+1]) of `records`, and k_r = (R_r - 2) * 16 / d must be
+ * 3, 4, 5 or 6.  Device-resident, AoS.
+ *   records  device, offsets[n_rows] bytes, 16-byte aligned.
+ *   offsets  device uint64[n_rows + 1], offsets[0] = 0, even, increasing;
+ *            borrowed for the handle's lifetime.
+ *   d        multiple of 32 in [32, 4096].
+ * The call checks every record length on the device and synchronises `stream`;
+ * CP_ERR_FORMAT if one gives no valid rate.  cp_lookup_decode then decodes the
+ * table (per-row rate); cp_lookup_decode_reduce and the SoA layout do not apply.
+ */
+cp_status cp_table_load_mixed(cp_table** out, const void* records, const uint64_t* offsets,
+                              uint64_t n_rows, uint32_t d, const uint16_t* lut_fp16, void* stream);
+
+/*
  * cp_lookup_decode -- e_hat_j = alpha_{r_j} * f(c_{r_j}) for the n requested
  * row ids r_j = idx[j], written as bf16 rows in lookup order, duplicates
  * included [P4 "how it differs"].  The table must be CP_RESIDENT_DEVICE.

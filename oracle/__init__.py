@@ -84,6 +84,9 @@ def lib():
         L.orc_lookup_decode_reduce.argtypes = [u8p, C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint64,
                                                u16p, i64p, C.c_uint64, C.c_uint32,
                                                C.POINTER(C.c_float), u16p, C.c_int]
+        L.orc_lookup_decode_mixed.restype = C.c_uint64
+        L.orc_lookup_decode_mixed.argtypes = [u8p, C.POINTER(C.c_uint64), C.c_uint64, C.c_uint32,
+                                              u16p, i64p, C.c_uint64, u16p]
         L.orc_distortion.restype = C.c_double
         L.orc_distortion.argtypes = [f64p, u8p, C.c_uint32, C.c_uint32, u16p]
         L.orc_encode_z.restype = C.c_double
@@ -185,6 +188,21 @@ def lookup_decode(records: np.ndarray, n_rows: int, d: int, k: int, rec_bytes: i
     bad = lib().orc_lookup_decode(_p(records, C.c_uint8), n_rows, d, k, rec_bytes,
                                   _p(lut, C.c_uint16), _p(idx, C.c_int64), idx.size,
                                   _p(out, C.c_uint16), n_threads)
+    return out, int(bad)
+
+
+def lookup_decode_mixed(records: np.ndarray, offsets: np.ndarray, d: int, lut: np.ndarray,
+                        idx: np.ndarray):
+    """bf16 bits (n, d) for a table with one bit rate per row (record r at
+    [offsets[r], offsets[r+1])), and the count of unusable ids."""
+    records = np.ascontiguousarray(records, dtype=np.uint8)
+    offsets = np.ascontiguousarray(offsets, dtype=np.uint64)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty((idx.size, d), dtype=np.uint16)
+    bad = lib().orc_lookup_decode_mixed(_p(records, C.c_uint8), _p(offsets, C.c_uint64),
+                                        offsets.size - 1, d, _p(lut, C.c_uint16),
+                                        _p(idx, C.c_int64), idx.size, _p(out, C.c_uint16))
     return out, int(bad)
 
 

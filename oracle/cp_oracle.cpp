@@ -591,6 +591,40 @@ uint64_t orc_lookup_decode(const uint8_t* records, uint64_t n_rows, uint32_t d, 
   return total;
 }
 
+// Lookup-decode of a table with a bit rate per row (frequency-based bit
+// allocation): record r occupies bytes [offsets[r], offsets[r+1]) and its rate
+// follows from its length, k_r = (R_r - 2) * 16 / d.  A record whose length
+// gives no k in {3, 4, 5, 6} decodes as a zero row and is counted like an
+// out-of-range id.  Returns that count.
+uint64_t orc_lookup_decode_mixed(const uint8_t* records, const uint64_t* offsets, uint64_t n_rows,
+                                 uint32_t d, const uint16_t* lut, const int64_t* idx, uint64_t n,
+                                 uint16_t* out) {
+  uint64_t bad = 0;
+  for (uint64_t j = 0; j < n; ++j) {
+    uint16_t* o = out + j * d;
+    const int64_t r = idx[j];
+    bool ok = r >= 0 && (uint64_t)r < n_rows;
+    uint64_t R = 0, k = 0;
+    if (ok) {
+      R = offsets[r + 1] - offsets[r];
+      ok = R >= 2 && ((R - 2) * 16) % d == 0;
+      if (ok) k = (R - 2) * 16 / d;
+      ok = ok && k >= 3 && k <= 6;
+    }
+    if (!ok) {
+      std::memset(o, 0, sizeof(uint16_t) * d);
+      bad += 1;
+      continue;
+    }
+    const Geometry g = make_geometry(d, (uint32_t)k);
+    const uint8_t* rec = records + offsets[r];
+    const uint64_t cb = R - 2;
+    const uint16_t a = (uint16_t)(rec[cb] | (rec[cb + 1] << 8));
+    reconstruct_row(rec, a, g, lut, o);
+  }
+  return bad;
+}
+
 // Decode fused with a weighted readout (the pages hand the rows to "the
 // existing readout"; this synthetic one sums each group of `group` consecutive
 // lookups): out[g][q] = bf16_rne(acc) with acc = 0 (fp32) and, for i in lookup

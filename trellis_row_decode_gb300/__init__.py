@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
-    "lookup_decode_reduce", "set_cache",
+    "lookup_decode_reduce", "set_cache", "load_mixed_table",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -74,6 +74,8 @@ def lib():
         L.cp_last_error.argtypes = []
         L.cp_test_inject_failure.restype = i32
         L.cp_test_inject_failure.argtypes = [i32, i32]
+        L.cp_table_load_mixed.restype = i32
+        L.cp_table_load_mixed.argtypes = [C.POINTER(vp), vp, vp, u64, u32, vp, vp]
         L.cp_table_set_cache.restype = i32
         L.cp_table_set_cache.argtypes = [vp, vp, u64, vp, vp]
         L.cp_lookup_decode_reduce.restype = i32
@@ -156,6 +158,24 @@ def load_table(records: torch.Tensor, n_rows: int, d: int, k: int, lut: np.ndarr
                          lut.ctypes.data, residency, layout, soa_ptr, _stream_ptr(stream))
     _check(st, "cp_table_load")
     return Table(h.value, n_rows, d, k, residency, layout, (records, soa, lut))
+
+
+def load_mixed_table(records: torch.Tensor, offsets: torch.Tensor, d: int,
+                     lut: np.ndarray | None = None, stream=None) -> Table:
+    """Bind a mixed-rate table: record r at records[offsets[r]:offsets[r+1]] (device
+    uint8 / int64 tensors); each row's rate follows from its record length."""
+    if not (records.is_cuda and offsets.is_cuda) or records.dtype != torch.uint8 \
+            or offsets.dtype != torch.int64:
+        raise ValueError("records (uint8) and offsets (int64) must be CUDA tensors")
+    if lut is None:
+        lut = default_lut()
+    lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    h = C.c_void_p(0)
+    n_rows = offsets.numel() - 1
+    st = lib().cp_table_load_mixed(C.byref(h), records.data_ptr(), offsets.data_ptr(), n_rows, d,
+                                   lut.ctypes.data, _stream_ptr(stream))
+    _check(st, "cp_table_load_mixed")
+    return Table(h.value, n_rows, d, 0, CP_RESIDENT_DEVICE, CP_LAYOUT_AOS, (records, offsets, lut))
 
 
 def _decode(fn, table: Table, idx: torch.Tensor, out: torch.Tensor | None, stream, what: str):

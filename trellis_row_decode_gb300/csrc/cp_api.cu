@@ -211,6 +211,47 @@ using cpx::kMaxLookups;
 using cpx::kMaxRows;
 using cpx::soa_stride;
 
+// Mixed-rate table: the HBM-path kernel with the rate chosen per row.
+cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
+                       cudaStream_t stream) {
+  cpk::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.codes = t->rec;
+  p.n_rows = t->n_rows;
+  p.table_bytes = t->table_bytes;
+  p.d = t->d;
+  p.code_bytes = t->d * 6 / 16;                         // stages sized for the widest rate
+  const uint32_t span = p.code_bytes + 2 + 14;
+  p.stage_bytes = cpk::kStagePrefix + ((span + 15u) & ~15u) + 16u;
+  p.lut = t->lut_dev;
+  p.idx = idx;
+  p.n = n;
+  p.out = out;
+  p.status = t->status_dev;
+  const int pf = cpk::kPfDevice;
+  int nwarps = cpk::kMaxWarps;
+  auto smem_for = [&](int w) {
+    return static_cast<size_t>(cpk::lut_bytes(32)) + static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
+  };
+  while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
+  const size_t smem = smem_for(nwarps);
+  if (smem > static_cast<size_t>(t->max_smem)) return CP_ERR_INVALID_ARG;
+  cpk::MixedFn fn = cpk::mixed_kernel(cpk::cpl_index(t->d));
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  uint64_t blocks = (n + nwarps - 1) / nwarps;
+  if (blocks > static_cast<uint64_t>(t->sm_count)) blocks = t->sm_count;
+  if (n / (blocks * nwarps) >= (1ull << 31)) return CP_ERR_INVALID_ARG;
+  const uint64_t* offsets = t->offsets;
+  void* args[] = {&p, &offsets};
+  e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
+                       dim3(nwarps * 32), args, smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mixed lookup-decode launch");
+  return CP_OK;
+}
+
 cp_status decode_common(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                         void* stream, int want_residency) {
   if (t == nullptr) return CP_ERR_INVALID_ARG;
@@ -232,6 +273,7 @@ cp_status decode_common(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     g_last_error = "current device differs from the table's device";
     return CP_ERR_INVALID_ARG;
   }
+  if (t->offsets != nullptr) return launch_mixed(t, idx, n, out, static_cast<cudaStream_t>(stream));
   const bool host = want_residency == CP_RESIDENT_HOST;
   cpx::HostScratch hs{};
   if (host) hs = cpx::host_scratch_layout(t->scratch_dev, cpk::kBucketChunk, t->bucket_nb);
@@ -462,6 +504,78 @@ cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t 
   return decode_common(t, idx, n, out, stream, CP_RESIDENT_HOST);
 }
 
+cp_status cp_table_load_mixed(cp_table** out, const void* records, const uint64_t* offsets,
+                              uint64_t n_rows, uint32_t d, const uint16_t* lut_fp16, void* stream) {
+  if (out == nullptr) return CP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (records == nullptr || offsets == nullptr || lut_fp16 == nullptr || n_rows == 0 ||
+      n_rows > kMaxRows || d < 32 || d > 4096 || d % 32 != 0 || !aligned(records, 16) ||
+      !aligned(offsets, 8)) {
+    cpx::set_error("bad records/offsets pointer or alignment, LUT pointer or geometry");
+    return CP_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < 1024; ++i) {
+    if ((lut_fp16[i] & 0x7c00u) == 0x7c00u) {
+      cpx::set_error("LUT holds a non-finite fp16 value");
+      return CP_ERR_FORMAT;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cp_table* t = new (std::nothrow) cp_table();
+  if (t == nullptr) return CP_ERR_NO_MEMORY;
+  cudaGetDevice(&t->device);
+  t->residency = CP_RESIDENT_DEVICE;
+  t->layout = CP_LAYOUT_AOS;
+  t->n_rows = n_rows;
+  t->d = d;
+  t->k = 0;
+  t->rec = static_cast<const uint8_t*>(records);
+  t->offsets = offsets;
+  cudaDeviceGetAttribute(&t->sm_count, cudaDevAttrMultiProcessorCount, t->device);
+  cudaDeviceGetAttribute(&t->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, t->device);
+  if (take_injected(g_fail_alloc)) {
+    cpx::set_error("injected device allocation failure");
+    delete t;
+    return CP_ERR_NO_MEMORY;
+  }
+  cudaError_t e = cudaMalloc(&t->lut_dev, 512 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&t->status_dev, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaMalloc");
+    cp_table_free(t);
+    return CP_ERR_NO_MEMORY;
+  }
+  e = cudaMemcpyAsync(t->lut_dev, lut_fp16, 2048, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(t->status_dev, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) {
+    cp_status st = cuda_fail(e, "LUT upload");
+    cp_table_free(t);
+    return st;
+  }
+  // every record length must give a rate in {3,..,6}; read the table's end
+  cpk::launch_check_mixed(offsets, n_rows, d, t->status_dev, t->sm_count, s);
+  uint32_t bad = 0;
+  uint64_t end = 0;
+  e = cudaMemcpyAsync(&bad, t->status_dev, sizeof(bad), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&end, offsets + n_rows, sizeof(end), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(t->status_dev, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cp_status st = cuda_fail(e, "mixed table check");
+    cp_table_free(t);
+    return st;
+  }
+  if (bad) {
+    cpx::set_error("a record length gives no bit rate in {3, 4, 5, 6} bits per step");
+    cp_table_free(t);
+    return CP_ERR_FORMAT;
+  }
+  t->table_bytes = end;
+  *out = t;
+  return CP_OK;
+}
+
 cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, void* cache,
                              void* stream) {
   if (t == nullptr) return CP_ERR_INVALID_ARG;
@@ -543,8 +657,8 @@ cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_
                                   uint32_t group, const float* weights, uint16_t* out,
                                   void* stream) {
   if (t == nullptr) return CP_ERR_INVALID_ARG;
-  if (t->residency != CP_RESIDENT_DEVICE) {
-    cpx::set_error("the fused readout needs a device-resident table");
+  if (t->residency != CP_RESIDENT_DEVICE || t->offsets != nullptr) {
+    cpx::set_error("the fused readout needs a device-resident single-rate table");
     return CP_ERR_INVALID_ARG;
   }
   if (n_groups == 0) return CP_OK;

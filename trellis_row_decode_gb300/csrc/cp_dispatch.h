@@ -20,6 +20,13 @@ constexpr int kLutRepHost = CP_LUTREP_HOST;
 
 using DecodeFn = void (*)(DecodeParams);
 using ReduceFn = void (*)(DecodeParams, const float*, uint32_t, uint64_t);
+using MixedFn = void (*)(DecodeParams, const uint64_t*);
+
+// Mixed-rate tables (one bit rate per row): kernel for a chunks-per-lane index
+// and the load-time check of the offset table (bad = 1 when a record is unusable).
+MixedFn mixed_kernel(int cpl_idx);
+void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
+                        int sm_count, cudaStream_t s);
 
 // Chunks-per-lane specialisations: index 0 = any d (runtime loop), index i > 0
 // = d == 256 * kCplValues[i].

@@ -25,6 +25,8 @@ struct cp_table {
   uint32_t* lut_dev;      // 512 words
   uint32_t* status_dev;   // 1 word
   void* scratch_dev;      // host-resident tables: see cpx::HostScratch (kBucketChunk capacity)
+  const uint64_t* offsets; // mixed-rate tables: record r at [offsets[r], offsets[r+1]), else null
+  uint64_t table_bytes;    // mixed-rate tables: offsets[n_rows]
   const uint8_t* cache;   // host-resident tables: device copies of hot records (cache_rows x R)
   uint64_t cache_rows;
   unsigned long long* cmap_keys;   // row id + 1 -> cache slot, open addressing (cmap_ts slots)

@@ -1,0 +1,43 @@
+// cp_mixed.cu -- mixed-rate tables: load-time check and kernel instantiations.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "cp_kernels_mixed.cuh"
+#include "cp_dispatch.h"
+
+namespace cpk {
+
+__global__ void check_mixed_offsets_kernel(const uint64_t* __restrict__ offsets, uint64_t n_rows,
+                                           uint32_t d, uint32_t* __restrict__ bad) {
+  const uint64_t T = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t r = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < n_rows; r += T) {
+    const uint64_t o0 = offsets[r], o1 = offsets[r + 1];
+    bool ok = o1 > o0 && (o0 & 1) == 0 && (r != 0 || o0 == 0);
+    if (ok) {
+      const uint64_t R = o1 - o0;
+      ok = R >= 2 && ((R - 2) * 16) % d == 0;
+      const uint64_t k = ok ? (R - 2) * 16 / d : 0;
+      ok = ok && k >= 3 && k <= 6;
+    }
+    if (!ok) *bad = 1u;
+  }
+}
+
+MixedFn mixed_kernel(int cpl_idx) {
+  switch (cpl_idx) {
+    case 1: return &lookup_decode_mixed_kernel<1>;
+    case 2: return &lookup_decode_mixed_kernel<2>;
+    case 3: return &lookup_decode_mixed_kernel<4>;
+    case 4: return &lookup_decode_mixed_kernel<8>;
+    case 5: return &lookup_decode_mixed_kernel<16>;
+    default: return &lookup_decode_mixed_kernel<0>;
+  }
+}
+
+void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
+                        int sm_count, cudaStream_t s) {
+  check_mixed_offsets_kernel<<<static_cast<unsigned>(sm_count) * 4, 256, 0, s>>>(offsets, n_rows,
+                                                                                  d, bad);
+}
+
+}  // namespace cpk

@@ -143,6 +143,36 @@ def fill_records(buf: torch.Tensor, seed: int, n_rows: int, d: int, k: int,
         view[r0:r1] = gen_records(seed, rows, d, k)
 
 
+def mixed_rates(seed: int, rows: torch.Tensor) -> torch.Tensor:
+    """Bits per step k in {3, 4, 5, 6} per row, uniform from hash bits (int64)."""
+    k = _subkeys(seed, 6)
+    return 3 + (lowbias32(_row_keys(seed, rows.to(torch.int64)) ^ k[5]) & 3)
+
+
+def mixed_offsets(ks: torch.Tensor, d: int) -> torch.Tensor:
+    """int64 [N + 1] byte offsets of records with rates ks (record = d*k/16 + 2 bytes)."""
+    sizes = ks.to(torch.int64) * (d // 16) + 2
+    off = torch.zeros(ks.numel() + 1, dtype=torch.int64, device=ks.device)
+    off[1:] = torch.cumsum(sizes, 0)
+    return off
+
+
+def fill_mixed_records(buf: torch.Tensor, seed: int, ks: torch.Tensor, offsets: torch.Tensor,
+                       d: int, chunk_rows: int = 1 << 18) -> None:
+    """Write row r's record (rate ks[r]) at buf[offsets[r]:offsets[r+1]]."""
+    n_rows = ks.numel()
+    for r0 in range(0, n_rows, chunk_rows):
+        r1 = min(n_rows, r0 + chunk_rows)
+        for k in (3, 4, 5, 6):
+            sel = torch.nonzero(ks[r0:r1] == k).flatten() + r0
+            if sel.numel() == 0:
+                continue
+            rec = gen_records(seed, sel.to(torch.int64), d, k)
+            R = rec.shape[1]
+            dst = offsets[sel][:, None] + torch.arange(R, device=buf.device)[None, :]
+            buf[dst.reshape(-1)] = rec.reshape(-1)
+
+
 # ---------------------------------------------------------------------------
 # Index streams (numpy, host).
 # ---------------------------------------------------------------------------

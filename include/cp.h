@@ -201,6 +201,29 @@ cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_
                                   void* stream);
 
 /*
+ * cp_encode_rows -- offline compression on the GPU: rows e -> AoS records.
+ * z = sqrt(d) e / |e| is coded by the tail-biting trellis (TCQ) and
+ * alpha = |e|_2 / |f(c)|_2 restores the norm [P4 "how it differs"].  Search:
+ * a free-start Viterbi on the sequence rotated by T/2 steps picks the 16 - k
+ * pre-window bits from its best path, then one Viterbi constrained to them
+ * gives a valid tail-biting code (the exact search, over every pre-window, is
+ * 2^(16-k) times costlier).  Precision (the pages fix none): |e|, z and alpha in
+ * fp64 with sums in index order, path metrics in fp32 (branch cost
+ * fl(fl((z0-y0)^2) + fl((z1-y1)^2)), no fused multiply-add); survivor per group
+ * of states sharing predecessors: smallest metric, then smallest dropped bits;
+ * final state: smallest metric, then smallest state.  A zero row gives a zero
+ * record.  Rows must be finite.
+ *   e        device fp32 [rows][d].
+ *   lut_fp16 host, 512 x (y0, y1) fp16 patterns (finite).
+ *   records  device, rows * R bytes (R = d*k/16 + 2).
+ *   cost     device fp32 [rows] (optional): the search's path metric.
+ * Allocates and frees its workspace (about 0.5 MB + d/2 * 2^(16-k) bytes per SM)
+ * and synchronises `stream` before returning.  d >= 16.
+ */
+cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d, uint32_t bits_per_step,
+                         const uint16_t* lut_fp16, uint8_t* records, float* cost, void* stream);
+
+/*
  * cp_get_status -- synchronise `stream`, then report and clear the table's
  * device status word: CP_ERR_INDEX_OOB if any decode since the last call saw an
  * out-of-range id, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK.

@@ -94,6 +94,14 @@ def lib():
         L.orc_encode_rows.restype = C.c_int
         L.orc_encode_rows.argtypes = [f64p, C.c_uint64, C.c_uint32, C.c_uint32, u16p, C.c_int,
                                       C.c_int, u8p, f64p, f64p]
+        f32p = C.POINTER(C.c_float)
+        L.orc_distortion_f32.restype = C.c_float
+        L.orc_distortion_f32.argtypes = [f32p, u8p, C.c_uint32, C.c_uint32, u16p]
+        L.orc_encode_z_f32.restype = C.c_float
+        L.orc_encode_z_f32.argtypes = [f32p, C.c_uint32, C.c_uint32, u16p, C.c_int, u8p]
+        L.orc_encode_rows_f32.restype = C.c_int
+        L.orc_encode_rows_f32.argtypes = [f32p, C.c_uint64, C.c_uint32, C.c_uint32, u16p, C.c_int,
+                                          u8p, f32p]
         L.orc_rtn2.restype = None
         L.orc_rtn2.argtypes = [f64p, C.c_uint32, C.c_int, f64p]
     return _lib
@@ -264,6 +272,42 @@ def encode_rows(e: np.ndarray, d: int, k: int, lut: np.ndarray, mode: int = TWO_
     if rc != 0:
         raise ValueError("encode_rows failed (geometry or mode)")
     return rec, alpha, cost
+
+
+def distortion_f32(z: np.ndarray, code: np.ndarray, d: int, k: int, lut: np.ndarray) -> float:
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    code = np.ascontiguousarray(code, dtype=np.uint8)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    return lib().orc_distortion_f32(_p(z, C.c_float), _p(code, C.c_uint8), d, k,
+                                    _p(lut, C.c_uint16))
+
+
+def encode_z_f32(z: np.ndarray, d: int, k: int, lut: np.ndarray, mode: int):
+    """fp32 search (the GPU encoder's precision): code and fp32 cost."""
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    code = np.zeros((d * k // 2 + 7) // 8, dtype=np.uint8)
+    cost = lib().orc_encode_z_f32(_p(z, C.c_float), d, k, _p(lut, C.c_uint16), mode,
+                                  _p(code, C.c_uint8))
+    if cost < 0:
+        raise ValueError("search mode does not apply to this geometry")
+    return code, cost
+
+
+def encode_rows_f32(e: np.ndarray, d: int, k: int, lut: np.ndarray,
+                    n_threads: int | None = None):
+    """AoS records (rows, d*k/16 + 2) from fp32 rows with the fp32 two-pass search, and costs."""
+    e = np.ascontiguousarray(e, dtype=np.float32).reshape(-1, d)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    rows = e.shape[0]
+    rec = np.zeros((rows, d * k // 16 + 2), dtype=np.uint8)
+    cost = np.empty(rows, dtype=np.float32)
+    rc = lib().orc_encode_rows_f32(_p(e, C.c_float), rows, d, k, _p(lut, C.c_uint16),
+                                   n_threads or n_threads_default(), _p(rec, C.c_uint8),
+                                   _p(cost, C.c_float))
+    if rc != 0:
+        raise ValueError("encode_rows_f32: geometry not supported")
+    return rec, cost
 
 
 def rtn2(e: np.ndarray, variant: int = 0) -> np.ndarray:

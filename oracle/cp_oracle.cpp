@@ -394,6 +394,186 @@ double viterbi_two_pass(const double* z, const Geometry& g, const StateTable& st
   return viterbi_fixed_w(z, g, st, w, code_out, wk);
 }
 
+// ---------------------------------------------------------------------------
+// fp32 variant of the encoder (the precision of the GPU encoder; the pages fix
+// none).  z comes from the fp64 normalisation rounded to fp32; branch cost
+// D = fl(fl((z0 - y0)^2) + fl((z1 - y1)^2)) in fp32 without fused multiply-adds;
+// path metrics in fp32.  Recursion per step: the 2^k states that share their
+// low W = 16 - k bits (a group g) also share their 2^k predecessors
+// (g << k) | y, so the survivor is chosen once per group, smallest predecessor
+// metric first, then smallest dropped bits y; every state of the group then
+// gets metric fl(min + D(s)).  Since fl(a + D) is monotone in a, the optimum
+// equals the minimum over all paths of their fp32 sums accumulated in t order.
+// ---------------------------------------------------------------------------
+
+struct StateTableF {
+  std::vector<float> y0, y1;
+};
+
+StateTableF make_state_table_f(const uint16_t* lut) {
+  StateTableF st;
+  st.y0.resize(kStates);
+  st.y1.resize(kStates);
+  for (uint32_t s = 0; s < kStates; ++s) {
+    double a, b;
+    state_values(s, lut, &a, &b);
+    st.y0[s] = (float)a;
+    st.y1[s] = (float)b;
+  }
+  return st;
+}
+
+inline float step_cost_f(const StateTableF& st, const float* z, uint32_t t, uint32_t s) {
+  const float a = z[2 * t] - st.y0[s];
+  const float b = z[2 * t + 1] - st.y1[s];
+  const float aa = a * a;
+  const float bb = b * b;
+  return aa + bb;
+}
+
+float distortion_f(const uint8_t* code, const Geometry& g, const StateTableF& st, const float* z) {
+  float acc = 0.0f;
+  for (uint32_t t = 0; t < g.T; ++t) acc = acc + step_cost_f(st, z, t, window_state(code, g, t));
+  return acc;
+}
+
+// One Viterbi pass in fp32 over steps t_0 .. t_{T-1} = (first + i) mod T.
+// init: metrics of the states before the first transition (step `first`);
+// force_w >= 0 constrains new bits in the w region (positions >= Lc - W) to w.
+// tb[i * 2^W + g] receives the chosen dropped bits of group g at pass step i.
+// Returns the final metrics.
+std::vector<float> viterbi_pass_f(const float* z, const Geometry& g, const StateTableF& st,
+                                  std::vector<float> cur, uint32_t first, int64_t force_w,
+                                  std::vector<uint8_t>& tb) {
+  const uint32_t k = g.k, T = g.T, Lc = g.Lc;
+  const uint32_t W = kStateBits - k;
+  const uint32_t groups = 1u << W;
+  const float inf = std::numeric_limits<float>::infinity();
+  std::vector<float> nxt(kStates);
+  tb.assign((size_t)T * groups, 0);
+  for (uint32_t i = 1; i < T; ++i) {
+    const uint32_t t = (first + i) % T;
+    uint32_t force_mask = 0, force_val = 0;
+    if (force_w >= 0) {
+      for (uint32_t b = 0; b < k; ++b) {
+        const uint64_t pos = (uint64_t)k * t + b;
+        if (pos >= (uint64_t)(Lc - W)) {
+          force_mask |= 1u << b;
+          force_val |= (((uint32_t)force_w >> (pos - (Lc - W))) & 1u) << b;
+        }
+      }
+    }
+    for (uint32_t grp = 0; grp < groups; ++grp) {
+      float best = cur[(size_t)grp << k];
+      uint32_t by = 0;
+      for (uint32_t y = 1; y < (1u << k); ++y) {
+        const float m = cur[((size_t)grp << k) | y];
+        if (m < best) {
+          best = m;
+          by = y;
+        }
+      }
+      tb[(size_t)i * groups + grp] = (uint8_t)by;
+      for (uint32_t x = 0; x < (1u << k); ++x) {
+        const uint32_t s = (x << W) | grp;
+        nxt[s] = ((x & force_mask) != force_val) ? inf : best + step_cost_f(st, z, t, s);
+      }
+    }
+    cur.swap(nxt);
+  }
+  return cur;
+}
+
+// Smallest finite metric, ties to the smaller state; -1 if none.
+int64_t argmin_state_f(const std::vector<float>& m) {
+  int64_t bs = -1;
+  for (uint32_t s = 0; s < kStates; ++s)
+    if (m[s] != std::numeric_limits<float>::infinity() && (bs < 0 || m[s] < m[bs])) bs = s;
+  return bs;
+}
+
+// Code of the path ending in state `fin` after a constrained pass from step 0.
+void traceback_code_f(const Geometry& g, const std::vector<uint8_t>& tb, uint32_t fin,
+                      uint8_t* code_out) {
+  const uint32_t k = g.k, W = kStateBits - k, groups = 1u << W;
+  std::memset(code_out, 0, (g.Lc + 7) / 8);
+  uint32_t s = fin;
+  for (int64_t t = g.T - 1; t >= 0; --t) {
+    const uint32_t x = s >> W;
+    for (uint32_t i = 0; i < k; ++i) set_code_bit(code_out, (uint64_t)k * t + i, (x >> i) & 1u);
+    if (t > 0) {
+      const uint32_t grp = s & (groups - 1);
+      s = (grp << k) | tb[(size_t)t * groups + grp];
+    }
+  }
+}
+
+// Constrained fp32 pass with pre-window w; returns the cost (inf if no path).
+float viterbi_fixed_w_f(const float* z, const Geometry& g, const StateTableF& st, uint32_t w,
+                        uint8_t* code_out) {
+  const uint32_t k = g.k, W = kStateBits - k;
+  std::vector<float> cur(kStates, std::numeric_limits<float>::infinity());
+  for (uint32_t x = 0; x < (1u << k); ++x) {
+    const uint32_t s = w | (x << W);
+    cur[s] = step_cost_f(st, z, 0, s);
+  }
+  std::vector<uint8_t> tb;
+  const std::vector<float> fin = viterbi_pass_f(z, g, st, cur, 0, (int64_t)w, tb);
+  const int64_t bs = argmin_state_f(fin);
+  if (bs < 0) return std::numeric_limits<float>::infinity();
+  traceback_code_f(g, tb, (uint32_t)bs, code_out);
+  return fin[bs];
+}
+
+float viterbi_exact_f(const float* z, const Geometry& g, const StateTableF& st, uint8_t* code_out) {
+  const uint32_t W = kStateBits - g.k;
+  const size_t nb = (g.Lc + 7) / 8;
+  std::vector<uint8_t> tmp(nb);
+  float best = std::numeric_limits<float>::infinity();
+  for (uint32_t w = 0; w < (1u << W); ++w) {
+    const float c = viterbi_fixed_w_f(z, g, st, w, tmp.data());
+    if (c < best) {
+      best = c;
+      std::memcpy(code_out, tmp.data(), nb);
+    }
+  }
+  return best;
+}
+
+// Two-pass fp32: free-start pass on the sequence rotated by T/2 steps, w read
+// off its best path at original step T-1, then one constrained pass.
+float viterbi_two_pass_f(const float* z, const Geometry& g, const StateTableF& st,
+                         uint8_t* code_out) {
+  const uint32_t k = g.k, T = g.T, W = kStateBits - k, groups = 1u << W;
+  const uint32_t rho = T / 2;
+  std::vector<float> cur(kStates);
+  for (uint32_t s = 0; s < kStates; ++s) cur[s] = step_cost_f(st, z, rho % T, s);
+  std::vector<uint8_t> tb;
+  const std::vector<float> fin = viterbi_pass_f(z, g, st, cur, rho, -1, tb);
+  uint32_t s = (uint32_t)argmin_state_f(fin);
+  const uint32_t target = T - 1 - rho;
+  for (uint32_t i = T - 1; i > target; --i) {
+    const uint32_t grp = s & (groups - 1);
+    s = (grp << k) | tb[(size_t)i * groups + grp];
+  }
+  return viterbi_fixed_w_f(z, g, st, s >> k, code_out);
+}
+
+float brute_force_f(const float* z, const Geometry& g, const StateTableF& st, uint8_t* code_out) {
+  const size_t nb = (g.Lc + 7) / 8;
+  std::vector<uint8_t> code(nb);
+  float best = std::numeric_limits<float>::infinity();
+  for (uint64_t c = 0; c < (1ull << g.Lc); ++c) {
+    for (size_t b = 0; b < nb; ++b) code[b] = (uint8_t)(c >> (8 * b));
+    const float D = distortion_f(code.data(), g, st, z);
+    if (D < best) {
+      best = D;
+      std::memcpy(code_out, code.data(), nb);
+    }
+  }
+  return best;
+}
+
 // Brute force over all 2^Lc codes (Lc <= 26): smallest cost, then smallest code.
 double brute_force(const double* z, const Geometry& g, const StateTable& st, uint8_t* code_out) {
   const size_t nb = (g.Lc + 7) / 8;
@@ -737,6 +917,69 @@ int orc_encode_rows(const double* e, uint64_t rows, uint32_t d, uint32_t k, cons
   for (auto& x : th) x.join();
   for (int f : fail)
     if (f) return -1;
+  return 0;
+}
+
+// fp32 encoder entry points (see the fp32 variant above).
+float orc_distortion_f32(const float* z, const uint8_t* code, uint32_t d, uint32_t k,
+                         const uint16_t* lut) {
+  const Geometry g = make_geometry(d, k);
+  const StateTableF st = make_state_table_f(lut);
+  return distortion_f(code, g, st, z);
+}
+
+float orc_encode_z_f32(const float* z, uint32_t d, uint32_t k, const uint16_t* lut, int mode,
+                       uint8_t* code_out) {
+  const Geometry g = make_geometry(d, k);
+  const StateTableF st = make_state_table_f(lut);
+  if (mode == ORC_BRUTE) return g.Lc > 26 ? -1.0f : brute_force_f(z, g, st, code_out);
+  if (g.Lc < (uint32_t)kStateBits) return -1.0f;
+  if (mode == ORC_EXACT) return viterbi_exact_f(z, g, st, code_out);
+  return viterbi_two_pass_f(z, g, st, code_out);
+}
+
+// Rows e (fp32 values, rows x d) -> AoS records with the fp32 two-pass search:
+// ss = sum e^2 (fp64, index order), nrm = sqrt(ss), z = (float)(e * (sqrt(d) / nrm));
+// alpha = nrm / sqrt(sum f^2) (fp64, index order) rounded once to bf16; a zero
+// row gets an all-zero code and alpha = 0.  cost (optional) receives the fp32
+// path metric.
+int orc_encode_rows_f32(const float* e, uint64_t rows, uint32_t d, uint32_t k, const uint16_t* lut,
+                        int n_threads, uint8_t* records, float* cost) {
+  const Geometry g = make_geometry(d, k);
+  if (g.Lc % 8 != 0 || g.Lc < (uint32_t)kStateBits) return -1;
+  const uint64_t code_bytes = g.Lc / 8, rec_bytes = code_bytes + 2;
+  const StateTableF st = make_state_table_f(lut);
+  if (n_threads < 1) n_threads = 1;
+  auto work = [&](int tid) {
+    std::vector<float> z(d);
+    std::vector<double> f(d);
+    for (uint64_t r = tid; r < rows; r += n_threads) {
+      const float* er = e + r * d;
+      uint8_t* rec = records + r * rec_bytes;
+      double ss = 0.0;
+      for (uint32_t q = 0; q < d; ++q) ss = ss + (double)er[q] * (double)er[q];
+      const double nrm = std::sqrt(ss);
+      if (nrm == 0.0) {
+        std::memset(rec, 0, rec_bytes);
+        if (cost) cost[r] = 0.0f;
+        continue;
+      }
+      const double sc = std::sqrt((double)d) / nrm;
+      for (uint32_t q = 0; q < d; ++q) z[q] = (float)((double)er[q] * sc);
+      const float c = viterbi_two_pass_f(z.data(), g, st, rec);
+      decode_f(rec, g, lut, f.data());
+      double fs = 0.0;
+      for (uint32_t q = 0; q < d; ++q) fs = fs + f[q] * f[q];
+      const uint16_t ab = double_to_bf16(nrm / std::sqrt(fs));
+      rec[code_bytes] = (uint8_t)(ab & 0xff);
+      rec[code_bytes + 1] = (uint8_t)(ab >> 8);
+      if (cost) cost[r] = c;
+    }
+  };
+  std::vector<std::thread> th;
+  for (int tI = 1; tI < n_threads; ++tI) th.emplace_back(work, tI);
+  work(0);
+  for (auto& x : th) x.join();
   return 0;
 }
 

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
-    "lookup_decode_reduce", "set_cache", "load_mixed_table",
+    "lookup_decode_reduce", "set_cache", "load_mixed_table", "encode_rows",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -74,6 +74,8 @@ def lib():
         L.cp_last_error.argtypes = []
         L.cp_test_inject_failure.restype = i32
         L.cp_test_inject_failure.argtypes = [i32, i32]
+        L.cp_encode_rows.restype = i32
+        L.cp_encode_rows.argtypes = [vp, u64, u32, u32, vp, vp, vp, vp]
         L.cp_table_load_mixed.restype = i32
         L.cp_table_load_mixed.argtypes = [C.POINTER(vp), vp, vp, u64, u32, vp, vp]
         L.cp_table_set_cache.restype = i32
@@ -240,6 +242,22 @@ def set_cache(table: Table, hot_rows, cache: torch.Tensor | None = None, stream=
     _check(lib().cp_table_set_cache(table.handle, rows.ctypes.data if m else None, m, ptr,
                                     _stream_ptr(stream)), "cp_table_set_cache")
     table._cache = cache if m else None
+
+
+def encode_rows(e: torch.Tensor, k: int, lut: np.ndarray | None = None, stream=None):
+    """GPU compression of fp32 rows e [rows, d] into AoS records (uint8 [rows, R]) and the
+    fp32 search costs; tail-biting two-pass Viterbi, norm-restoring bf16 alpha."""
+    if not e.is_cuda or e.dtype != torch.float32 or e.dim() != 2 or not e.is_contiguous():
+        raise ValueError("e must be a contiguous 2-D float32 CUDA tensor")
+    rows, d = e.shape
+    if lut is None:
+        lut = default_lut()
+    lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    rec = torch.empty((rows, record_bytes(d, k)), dtype=torch.uint8, device=e.device)
+    cost = torch.empty(rows, dtype=torch.float32, device=e.device)
+    _check(lib().cp_encode_rows(e.data_ptr(), rows, d, k, lut.ctypes.data, rec.data_ptr(),
+                                cost.data_ptr(), _stream_ptr(stream)), "cp_encode_rows")
+    return rec, cost
 
 
 def get_status(table: Table, stream=None) -> int:

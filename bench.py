@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip timing the other table configs (mid, bit-rate sweep, decode step)")
     return ap.parse_args()
 
 
@@ -319,6 +321,10 @@ def our_arm(args, w, rank, world, local):
     achieved = n * bpl / float(t.mean()) / 1e9
     peak, peak_kind = measured_peaks()
 
+    others = None
+    if rank == 0 and not args.no_other_configs:
+        others = other_configs(args, w, table, idx, out, flush, stream)
+
     # Decode fused with a weighted readout over each token's 24 rows of a layer.
     fused = None
     if w.d in (256, 512, 1024) and w.rows_per_token % 24 == 0:
@@ -444,10 +450,70 @@ def our_arm(args, w, rank, world, local):
             line["mixed_rate"] = mixed
         if enc is not None:
             line["encoder"] = enc
+        if others is not None:
+            line["other_configs"] = others
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+OTHER_CONFIGS = ("mid", "sweep_b1.5", "sweep_b2", "sweep_b2.5", "sweep_b3", "deepseek_decode")
+
+
+def other_configs(args, w, table, idx, out, flush, stream):
+    """Median step of cp_lookup_decode on the other table configs (HBM, AoS):
+    the 2^24-row d=512 table, the d=1024 bit-rate sweep, the decode step of 2048
+    sequences x 48 rows on the main table, and the prefill replay issued as one
+    call per layer (token-major ids [token][layer][24])."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    steps = min(args.steps, 300)
+    peak = measured_peaks()[0]
+    res = {}
+
+    def entry(ow, n, tm):
+        bpl = ow.algorithmic_bytes_per_lookup()
+        return {"lookups": n, "d": ow.d, "b": ow.k / 2, "n_rows": ow.n_rows,
+                "ms_per_step": tm * 1e3, "rows_per_s": n / tm,
+                "algorithmic_gbs": n * bpl / tm / 1e9, "frac_of_hbm_peak": n * bpl / tm / 1e9 / peak}
+
+    for name in OTHER_CONFIGS:
+        ow = synth.WORKLOADS[name]
+        if name == w.name:
+            continue
+        same_table = (ow.n_rows, ow.d, ow.k) == (w.n_rows, w.d, w.k)
+        if not same_table and ow.table_bytes > (16 << 30):
+            continue
+        tab, rec, _ = (table, None, None) if same_table else build_table(ow, "aos", synth.SEED_TABLE)
+        oidx = torch.from_numpy(ow.indices()).cuda()
+        oout = torch.empty((oidx.numel(), ow.d), dtype=torch.bfloat16, device="cuda")
+        t = time_steps(lambda: cp.lookup_decode(tab, oidx, oout, stream), steps, args.warmup,
+                       flush, stream)
+        assert cp.get_status(tab) == cp.CP_OK
+        res[name] = entry(ow, oidx.numel(), float(np.median(t)))
+        if not same_table:
+            tab.close()
+        del rec, oidx, oout
+        torch.cuda.empty_cache()
+
+    # the same replay as two calls, one per layer of 24 rows per token
+    if w.rows_per_token == 48:
+        lay = idx.view(w.tokens, 2, 24)
+        parts = [lay[:, l, :].contiguous().view(-1) for l in range(2)]
+        outs = [out[: p.numel()] for p in parts]
+        outs[1] = out[parts[0].numel():]
+
+        def two():
+            cp.lookup_decode(table, parts[0], outs[0], stream)
+            cp.lookup_decode(table, parts[1], outs[1], stream)
+        t = time_steps(two, steps, args.warmup, flush, stream)
+        assert cp.get_status(table) == cp.CP_OK
+        e = entry(w, idx.numel(), float(np.median(t)))
+        e["calls_per_step"] = 2
+        res[w.name + " (one call per layer)"] = e
+    return res
 
 
 def host_path_measure(args, w, idx, flush, stream):

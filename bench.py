@@ -370,7 +370,7 @@ def our_arm(args, w, rank, world, local):
     # Offline compression on the GPU (the step before the hot path): 2 x SMs rows.
     enc = None
     if rank == 0 and w.d >= 16:
-        erows = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+        erows = 4 * torch.cuda.get_device_properties(0).multi_processor_count
         e_in = torch.from_numpy(synth.normal_rows(synth.SEED_ENCODER_ROWS, erows, w.d)
                                 .astype(np.float32)).cuda()
         cp.encode_rows(e_in[: erows // 2], w.k)                # warm-up

@@ -15,9 +15,15 @@
 // smallest dropped bits) and every state of the group adds its branch cost;
 // one traceback byte per group and step.
 //
-// Work mapping: one CTA of 1024 threads per row (persistent over rows); the
-// 2^16 path metrics (two 256 KB buffers) and the traceback bytes live in a
-// per-CTA global scratch that stays in L2; the LUT and z sit in shared memory.
+// Work mapping: one cluster of 4 CTAs x 1024 threads per row (persistent over
+// rows).  CTA c owns the 2^14 states whose top two bits are c, 16 per thread,
+// held in registers.  The predecessors of a group are 2^K consecutive states, so
+// the group minima are local; the 2^W group minima are what every CTA needs for
+// the next step and are pushed to all four CTAs through distributed shared
+// memory, one cluster barrier per step.  The branch cost depends on the state
+// only through its signed LUT entry, so each step first tabulates the 1024
+// possible costs in shared memory (replicated against bank conflicts).  The
+// traceback bytes (one per group and step) go to a per-cluster global scratch.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
@@ -28,8 +34,17 @@ namespace cpk {
 
 namespace {
 
-constexpr int kEncThreads = 1024;
+#ifndef CP_ENC_THREADS
+#define CP_ENC_THREADS 1024
+#endif
+constexpr int kEncThreads = CP_ENC_THREADS;                    // 512 or 1024
 constexpr uint32_t kStates = 1u << 16;
+constexpr uint32_t kCluster = 4;
+constexpr uint32_t kLocalStates = kStates / kCluster;          // 2^14 per CTA
+constexpr int kPerThread = kLocalStates / kEncThreads;        // states per thread (32 or 16)
+static_assert(kPerThread == 16 || kPerThread == 32, "512 or 1024 threads");
+constexpr int kCostRep = 8;                                    // cost table replicas
+constexpr uint32_t kCostBytes = 1024u * kCostRep * 4;          // one step's table
 
 struct EncodeParams {
   const float* e;           // rows x d, fp32
@@ -38,8 +53,8 @@ struct EncodeParams {
   const uint32_t* lut;      // 512 words: fp16 y0 | fp16 y1 << 16
   uint8_t* records;         // rows x R
   float* cost;              // rows (optional)
-  uint8_t* work;            // per CTA: 2 x 2^16 floats, then T x 2^W traceback bytes
-  uint64_t work_stride;     // bytes per CTA
+  uint8_t* work;            // per cluster: T x 2^W traceback bytes
+  uint64_t work_stride;     // bytes per cluster
 };
 
 // Round a positive or zero double to bf16 (one rounding, ties to even).
@@ -66,151 +81,348 @@ __device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
   return static_cast<uint16_t>(((e8 + 127) << 7) | (m8 & 0x7F));
 }
 
-// (y0, y1) of state s as fp32 (exact fp16 values), the sign of y1 from hash bit 23.
-__device__ __forceinline__ float2 state_y(const uint32_t* lut, uint32_t s) {
-  const uint32_t h = s * s + s;
-  uint32_t v = lut[(h >> 14) & 511];
-  if ((h >> 23) & 1u) v ^= 0x80000000u;
+// (y0, y1) of signed LUT entry e (bit 9 = sign of y1) as fp32 (exact fp16 values).
+__device__ __forceinline__ float2 entry_y(const uint32_t* lut, uint32_t e) {
+  uint32_t v = lut[e & 511];
+  if (e & 512) v ^= 0x80000000u;
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
-__device__ __forceinline__ float branch_cost(const uint32_t* lut, const float* z, uint32_t t,
-                                             uint32_t s) {
-  const float2 y = state_y(lut, s);
-  const float a = __fsub_rn(z[2 * t], y.x);
-  const float b = __fsub_rn(z[2 * t + 1], y.y);
+// Signed LUT entry of state s: (h >> 14) & 1023 with h = s*s + s; its bit 9 is
+// hash bit 23, the sign of y1.
+__device__ __forceinline__ uint32_t state_entry(uint32_t s) { return ((s * s + s) >> 14) & 1023u; }
+
+// fl(fl((z0 - y0)^2) + fl((z1 - y1)^2)), no contraction.
+__device__ __forceinline__ float pair_cost(float z0, float z1, float2 y) {
+  const float a = __fsub_rn(z0, y.x);
+  const float b = __fsub_rn(z1, y.y);
   return __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
 }
 
-// CTA-wide argmin over 2^16 metrics: smallest finite value, ties to the smaller
-// state; returns -1 (as 0xFFFFFFFF) when every metric is infinite.
-__device__ uint32_t cta_argmin(const float* m, float* red_v, uint32_t* red_s, float* best_out) {
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float bv = INFINITY;
-  uint32_t bs = 0xFFFFFFFFu;
-  for (uint32_t s = tid; s < kStates; s += kEncThreads) {
-    const float v = m[s];
-    if (v < bv) {                        // states of a thread ascend: strict < keeps the smaller
-      bv = v;
-      bs = s;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_down_sync(0xffffffffu, bv, o);
-    const uint32_t os = __shfl_down_sync(0xffffffffu, bs, o);
-    if (ov < bv || (ov == bv && os < bs)) {
-      bv = ov;
-      bs = os;
-    }
-  }
-  if (lane == 0) {
-    red_v[warp] = bv;
-    red_s[warp] = bs;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    bv = red_v[lane];
-    bs = red_s[lane];
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_down_sync(0xffffffffu, bv, o);
-      const uint32_t os = __shfl_down_sync(0xffffffffu, bs, o);
-      if (ov < bv || (ov == bv && os < bs)) {
-        bv = ov;
-        bs = os;
-      }
-    }
-    if (lane == 0) {
-      red_v[0] = bv;
-      red_s[0] = bs;
-    }
-  }
-  __syncthreads();
-  const uint32_t r = (red_v[0] == INFINITY) ? 0xFFFFFFFFu : red_s[0];
-  *best_out = red_v[0];
-  __syncthreads();
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// All threads of the cluster; orders shared (local and remote) and global accesses.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Address of local shared address `a` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_peer(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 
-// One pass over steps first+1 .. first+T-1 (mod T), cur holding the metrics of
-// the states of step `first`; force_w >= 0 pins new bits in the w region.
-template <int K>
-__device__ float* viterbi_pass(const uint32_t* lut, const float* z, uint32_t T, uint32_t Lc,
-                               float* cur, float* nxt, uint8_t* tb, uint32_t first,
-                               int64_t force_w) {
-  constexpr uint32_t W = 16 - K;
-  constexpr uint32_t kGroups = 1u << W;
-  const uint32_t tid = threadIdx.x;
-  for (uint32_t i = 1; i < T; ++i) {
-    const uint32_t t = (first + i) % T;
-    uint32_t fmask = 0, fval = 0;
-    if (force_w >= 0) {
-      for (uint32_t b = 0; b < K; ++b) {
-        const uint32_t pos = K * t + b;
-        if (pos >= Lc - W) {
-          fmask |= 1u << b;
-          fval |= ((static_cast<uint32_t>(force_w) >> (pos - (Lc - W))) & 1u) << b;
-        }
-      }
-    }
-    uint8_t* tbi = tb + static_cast<size_t>(i) * kGroups;
-    for (uint32_t g = tid; g < kGroups; g += kEncThreads) {
-      const float* pr = cur + (static_cast<size_t>(g) << K);
-      float best = pr[0];
-      uint32_t by = 0;
-#pragma unroll
-      for (uint32_t y = 1; y < (1u << K); ++y) {
-        const float m = pr[y];
-        if (m < best) {
-          best = m;
-          by = y;
-        }
-      }
-      tbi[g] = static_cast<uint8_t>(by);
-#pragma unroll 4
-      for (uint32_t x = 0; x < (1u << K); ++x) {
-        const uint32_t s = (x << W) | g;
-        nxt[s] = ((x & fmask) != fval) ? INFINITY : __fadd_rn(best, branch_cost(lut, z, t, s));
-      }
-    }
-    __syncthreads();
-    float* tmp = cur;
-    cur = nxt;
-    nxt = tmp;
+// Word index of group g's minimum in the group-minimum array: 16-byte units are
+// XOR-swizzled within blocks of eight, so the 16-byte reads of consecutive
+// groups (16 or 32 per thread) are free of bank conflicts across a quarter warp.
+__device__ __forceinline__ uint32_t best_word(uint32_t g) {
+  const uint32_t u = g >> 2;
+  return ((u ^ ((u >> 3) & 7u)) << 2) | (g & 3u);
+}
+
+// Lexicographic (value, index) minimum; strict so equal values keep the smaller index.
+__device__ __forceinline__ void min_pair(float& v, uint32_t& i, float ov, uint32_t oi) {
+  if (ov < v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
   }
-  return cur;
+}
+
+// Branch costs of step t for the 1024 signed entries, kCostRep copies each
+// (entry e, copy r at word e * kCostRep + r).
+__device__ __forceinline__ void build_costs(float* ct, const uint32_t* lut, const float* z,
+                                            uint32_t t) {
+  const float z0 = z[2 * t], z1 = z[2 * t + 1];
+#pragma unroll
+  for (uint32_t e = threadIdx.x; e < 1024; e += kEncThreads) {
+    const float c = pair_cost(z0, z1, entry_y(lut, e));
+    float4* dst = reinterpret_cast<float4*>(ct + e * kCostRep);
+#pragma unroll
+    for (int r = 0; r < kCostRep / 4; ++r) dst[r] = make_float4(c, c, c, c);
+  }
+}
+
+// Byte offset of state s's cost in a table, copy (lane % kCostRep).
+__device__ __forceinline__ uint32_t cost_off(uint32_t s, uint32_t lane_off) {
+  constexpr int kSh = 14 - 5;                          // entry * kCostRep * 4 = entry << 5
+  static_assert(kCostRep * 4 == 32, "shift assumes 8 copies");
+  return (((s * s + s) >> kSh) & (1023u << 5)) | lane_off;
+}
+
+// Per-CTA shared memory (offsets in bytes from the dynamic base).
+struct EncSmem {
+  uint32_t ct, best, lut, z, code, red, slots, total;
+};
+
+__host__ __device__ inline EncSmem enc_smem(uint32_t d, uint32_t k) {
+  EncSmem m;
+  const uint32_t W = 16 - k;
+  m.ct = 0;                                            // 3 x cost table; also fp64 scratch
+  m.best = 3 * kCostBytes;                             // 2 x 2^W floats
+  m.lut = m.best + 2 * (4u << W);
+  m.z = m.lut + 2048;
+  m.code = m.z + 4 * d;
+  m.red = m.code + ((d * k / 16 + 15) & ~15u);         // 32 floats + 32 words
+  m.slots = m.red + 256;                               // 4 floats, 4 words, w, 2 doubles
+  m.total = m.slots + 64;
+  return m;
 }
 
 template <int K>
 __global__ void __launch_bounds__(kEncThreads, 1) tcq_encode_kernel(const EncodeParams p) {
   constexpr uint32_t W = 16 - K;
-  constexpr uint32_t kGroups = 1u << W;
+  constexpr uint32_t kMask = (1u << W) - 1;
+  // own groups: a thread's states are NG whole groups of GS, or 1/SPLIT of one group
+  constexpr int GS = (1 << K) < kPerThread ? (1 << K) : kPerThread;
+  constexpr int NG = kPerThread / GS;
+  constexpr int SPLIT = (1 << K) / GS;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* lut = reinterpret_cast<uint32_t*>(smem);                  // 512 words
-  float* red_v = reinterpret_cast<float*>(smem + 2048);               // 32
-  uint32_t* red_s = reinterpret_cast<uint32_t*>(smem + 2048 + 128);   // 32
-  double* sh_d = reinterpret_cast<double*>(smem + 2048 + 256);        // 4 doubles
-  uint32_t* sh_u = reinterpret_cast<uint32_t*>(smem + 2048 + 288);    // 4 words
-  float* z = reinterpret_cast<float*>(smem + 2048 + 304);             // d floats
-  uint8_t* code = smem + 2048 + 304 + 4 * p.d;                        // Lc / 8 bytes
-
-  const uint32_t tid = threadIdx.x;
   const uint32_t d = p.d, T = d / 2, Lc = K * T, code_bytes = Lc / 8;
+  const EncSmem L = enc_smem(d, K);
+  float* ct = reinterpret_cast<float*>(smem + L.ct);
+  float* best = reinterpret_cast<float*>(smem + L.best);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut);
+  float* z = reinterpret_cast<float*>(smem + L.z);
+  uint8_t* code = smem + L.code;
+  float* red_v = reinterpret_cast<float*>(smem + L.red);
+  uint32_t* red_s = reinterpret_cast<uint32_t*>(smem + L.red + 128);
+  float* slot_v = reinterpret_cast<float*>(smem + L.slots);
+  uint32_t* slot_s = reinterpret_cast<uint32_t*>(smem + L.slots + 16);
+  uint32_t* slot_w = reinterpret_cast<uint32_t*>(smem + L.slots + 32);
+  double* sh_d = reinterpret_cast<double*>(smem + L.slots + 48);
+  double* scratch = reinterpret_cast<double*>(smem + L.ct);
+
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t crank = cluster_rank();
+  const uint32_t base = crank * kLocalStates + tid * kPerThread;   // this thread's states
+  const uint32_t lane_off = (lane & (kCostRep - 1)) * 4;
+  const uint32_t best_sa = smem_u32(best);
+  const uint32_t slots_sa = smem_u32(smem + L.slots);
+  // per-thread constants: cluster addresses of the group-minimum buffers, own
+  // groups' word offsets, the swizzle of the thread's 16-byte reads
+  uint32_t peer_best[2][kCluster];
+#pragma unroll
+  for (uint32_t b = 0; b < 2; ++b)
+#pragma unroll
+    for (uint32_t c = 0; c < kCluster; ++c) peer_best[b][c] = peer_addr(best_sa + b * (4u << W), c);
+  // the thread reads groups (base & kMask) + [0, kPerThread): 16-byte units u0 + q4,
+  // all in one block of eight, so their swizzle (u >> 3) & 7 is the same
+  const uint32_t u0 = (base & kMask) >> 2;
+  const uint32_t rd_swz = (u0 >> 3) & 7u;
   for (uint32_t i = tid; i < 512; i += kEncThreads) lut[i] = p.lut[i];
-  float* cur = reinterpret_cast<float*>(p.work + blockIdx.x * p.work_stride);
-  float* nxt = cur + kStates;
-  uint8_t* tb = reinterpret_cast<uint8_t*>(nxt + kStates);
+  uint8_t* tb = p.work + static_cast<uint64_t>(cluster_index()) * p.work_stride;
   __syncthreads();
 
-  for (uint64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+  float v[kPerThread] = {};
+
+  // Step i of a pass (steps t(1), t(2), ... after the start step t(0)): group
+  // minima of v (metrics at t(i-1)) -> traceback bytes and the minima in every
+  // CTA's buffer i & 1; then the new metrics at t(i) = tcur.  The cost table of
+  // t(i) was built one step earlier (table i % 3); this step builds the one of
+  // t(i+1) = tnext and reads its own costs while the cluster barrier completes.
+  // Reuse: table (i+1) % 3 and buffer i & 1 were last read at step i-2, before
+  // every thread's arrival at step i-1.
+  auto step = [&](uint32_t i, uint32_t tcur, uint32_t tnext, bool build_next, bool forced_pass,
+                  uint32_t w) {
+    const uint32_t buf = i & 1;
+    uint32_t tbv[NG];
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      float bv = v[gi * GS];
+      uint32_t by = 0;
+#pragma unroll
+      for (int y = 1; y < GS; ++y) {
+        if (v[gi * GS + y] < bv) {
+          bv = v[gi * GS + y];
+          by = y;
+        }
+      }
+      if constexpr (SPLIT > 1) {
+        by += base & ((1u << K) - 1);
+#pragma unroll
+        for (int o = 1; o < SPLIT; o <<= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const uint32_t oy = __shfl_xor_sync(0xffffffffu, by, o);
+          min_pair(bv, by, ov, oy);
+        }
+      }
+      tbv[gi] = by;
+      if (SPLIT == 1 || (tid & (SPLIT - 1)) == 0) {
+        const uint32_t off = 4 * best_word((base >> K) + gi);
+#pragma unroll
+        for (uint32_t c = 0; c < kCluster; ++c)
+          st_peer((buf ? peer_best[1][c] : peer_best[0][c]) + off, __float_as_uint(bv));
+      }
+    }
+    if (build_next) build_costs(ct + ((i + 1) % 3) * (kCostBytes / 4), lut, z, tnext);
+    cluster_arrive();
+    // traceback bytes (global) after the arrival, so its release does not wait for them
+    if (SPLIT == 1 || (tid & (SPLIT - 1)) == 0) {
+      uint8_t* tbi = tb + static_cast<uint64_t>(i) * (kMask + 1) + (base >> K);
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) tbi[gi] = static_cast<uint8_t>(tbv[gi]);
+    }
+    // own costs at t(i), from the table built before the previous barrier
+    const uint8_t* ctb = reinterpret_cast<const uint8_t*>(ct + (i % 3) * (kCostBytes / 4));
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q)
+      v[q] = *reinterpret_cast<const float*>(ctb + cost_off(base + q, lane_off));
+    // forced new bits (second pass): positions >= Lc - W hold w; the new bits
+    // (base >> W) are the same for all of the thread's states
+    bool dead = false;
+    if (forced_pass && K * tcur + K > Lc - W) {
+      uint32_t fmask = 0, fval = 0;
+      for (uint32_t b = 0; b < K; ++b) {
+        const uint32_t pos = K * tcur + b;
+        if (pos >= Lc - W) {
+          fmask |= 1u << b;
+          fval |= ((w >> (pos - (Lc - W))) & 1u) << b;
+        }
+      }
+      dead = ((base >> W) & fmask) != fval;
+    }
+    cluster_wait();
+    const float* bb = best + buf * (1u << W);
+#pragma unroll
+    for (int q4 = 0; q4 < kPerThread / 4; ++q4) {
+      float4 b4 = *reinterpret_cast<const float4*>(bb + 4 * ((u0 + q4) ^ rd_swz));
+      if (dead) b4 = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+      v[4 * q4] = __fadd_rn(b4.x, v[4 * q4]);
+      v[4 * q4 + 1] = __fadd_rn(b4.y, v[4 * q4 + 1]);
+      v[4 * q4 + 2] = __fadd_rn(b4.z, v[4 * q4 + 2]);
+      v[4 * q4 + 3] = __fadd_rn(b4.w, v[4 * q4 + 3]);
+    }
+  };
+
+  // Cluster-wide argmin of v: smallest finite value, ties to the smaller state;
+  // state 0xFFFFFFFF when every metric is infinite.  Ends with a cluster barrier.
+  auto argmin = [&](float* best_v) -> uint32_t {
+    float bv = INFINITY;
+    uint32_t bs = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      if (v[q] < bv) {
+        bv = v[q];
+        bs = base + q;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const uint32_t os = __shfl_xor_sync(0xffffffffu, bs, o);
+      min_pair(bv, bs, ov, os);
+    }
+    if (lane == 0) {
+      red_v[warp] = bv;
+      red_s[warp] = bs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      constexpr uint32_t kWarps = kEncThreads / 32;
+      bv = lane < kWarps ? red_v[lane] : INFINITY;
+      bs = lane < kWarps ? red_s[lane] : 0xFFFFFFFFu;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const uint32_t os = __shfl_xor_sync(0xffffffffu, bs, o);
+        min_pair(bv, bs, ov, os);
+      }
+      if (lane < kCluster) {
+        st_peer(peer_addr(slots_sa + 4 * crank, lane), __float_as_uint(bv));
+        st_peer(peer_addr(slots_sa + 16 + 4 * crank, lane), bs);
+      }
+    }
+    cluster_sync();
+    bv = slot_v[0];
+    bs = slot_s[0];
+#pragma unroll
+    for (uint32_t c = 1; c < kCluster; ++c) min_pair(bv, bs, slot_v[c], slot_s[c]);
+    *best_v = bv;
+    return (bv == INFINITY) ? 0xFFFFFFFFu : bs;
+  };
+
+  auto start_costs = [&]() {                          // v = costs of step t(0) (table 0)
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q)
+      v[q] = *reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(ct) +
+                                             cost_off(base + q, lane_off));
+  };
+
+  // Traceback by the CTA (rank 0 only): from state s at step index hi down to
+  // step index lo + 1, stepping back s <- (g << K) | tb[i][g] (g = low W bits).
+  // Chunks of traceback rows are copied into shared memory (the cost tables'
+  // space, free between passes) by all threads; thread 0 walks them.  With
+  // `emit`, thread 0 also writes the new bits of each step (top K bits of s at
+  // step i) into code.  Returns the state at step lo (valid in thread 0).
+  auto walk = [&](uint32_t s, uint32_t hi, uint32_t lo, bool emit) -> uint32_t {
+    constexpr uint32_t kRowBytes = 1u << W;
+    const uint32_t chunk = (3 * kCostBytes) / kRowBytes;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(ct);
+    for (uint32_t c_hi = hi; c_hi > lo;) {
+      const uint32_t c_lo = (c_hi - lo > chunk) ? c_hi - chunk + 1 : lo + 1;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(tb + static_cast<uint64_t>(c_lo) * kRowBytes);
+      const uint32_t n16 = (c_hi - c_lo + 1) * (kRowBytes / 16);
+      for (uint32_t q = tid; q < n16; q += kEncThreads)
+        reinterpret_cast<uint4*>(stage)[q] = __ldcg(src + q);
+      __syncthreads();
+      if (tid == 0) {
+        for (uint32_t i = c_hi; i >= c_lo; --i) {
+          if (emit) {
+            const uint32_t x = s >> W;
+            for (uint32_t b = 0; b < K; ++b) {
+              const uint32_t j = K * i + b;
+              if ((x >> b) & 1u) code[j >> 3] |= static_cast<uint8_t>(1u << (j & 7));
+            }
+          }
+          const uint32_t g = s & kMask;
+          s = (g << K) | stage[(i - c_lo) * kRowBytes + g];
+        }
+      }
+      __syncthreads();
+      c_hi = c_lo - 1;
+    }
+    return s;
+  };
+
+  for (uint64_t r = cluster_index(); r < p.rows; r += cluster_count()) {
     const float* er = p.e + r * d;
     uint8_t* rec = p.records + r * (code_bytes + 2);
     // |e| and z = (float)(e * sqrt(d) / |e|) in fp64, sums in index order
+    for (uint32_t q = tid; q < d; q += kEncThreads) {
+      const double x = static_cast<double>(er[q]);
+      scratch[q] = __dmul_rn(x, x);
+    }
+    __syncthreads();
     if (tid == 0) {
       double ss = 0.0;
-      for (uint32_t q = 0; q < d; ++q) {
-        const double v = static_cast<double>(er[q]);
-        ss = __dadd_rn(ss, __dmul_rn(v, v));
-      }
+      for (uint32_t q = 0; q < d; ++q) ss = __dadd_rn(ss, scratch[q]);
       const double nrm = __dsqrt_rn(ss);
       sh_d[0] = nrm;
       sh_d[1] = (nrm == 0.0) ? 0.0 : __ddiv_rn(__dsqrt_rn(static_cast<double>(d)), nrm);
@@ -218,8 +430,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) tcq_encode_kernel(const Encode
     __syncthreads();
     const double nrm = sh_d[0], sc = sh_d[1];
     if (nrm == 0.0) {                                   // zero row: zero code, alpha = 0
-      for (uint32_t i = tid; i < code_bytes + 2; i += kEncThreads) rec[i] = 0;
-      if (tid == 0 && p.cost) p.cost[r] = 0.0f;
+      if (crank == 0) {
+        for (uint32_t i = tid; i < code_bytes + 2; i += kEncThreads) rec[i] = 0;
+        if (tid == 0 && p.cost) p.cost[r] = 0.0f;
+      }
       __syncthreads();
       continue;
     }
@@ -229,55 +443,48 @@ __global__ void __launch_bounds__(kEncThreads, 1) tcq_encode_kernel(const Encode
 
     // pass 1: free start at step rho = T/2, every state live
     const uint32_t rho = T / 2;
-    for (uint32_t s = tid; s < kStates; s += kEncThreads) cur[s] = branch_cost(lut, z, rho, s);
+    build_costs(ct, lut, z, rho);
+    build_costs(ct + kCostBytes / 4, lut, z, (rho + 1) % T);
     __syncthreads();
-    float* fin = viterbi_pass<K>(lut, z, T, Lc, cur, nxt, tb, rho, -1);
+    start_costs();
+    for (uint32_t i = 1; i < T; ++i)
+      step(i, (rho + i) % T, (rho + i + 1) % T, i + 1 < T, false, 0);
     float bestv;
-    uint32_t bs = cta_argmin(fin, red_v, red_s, &bestv);
-    if (tid == 0) {                                     // walk back to original step T-1
-      uint32_t s = bs;
-      const uint32_t target = T - 1 - rho;
-      for (uint32_t i = T - 1; i > target; --i) {
-        const uint32_t g = s & (kGroups - 1);
-        s = (g << K) | tb[static_cast<size_t>(i) * kGroups + g];
-      }
-      sh_u[0] = s >> K;                                 // the pre-window bits w
+    uint32_t bs = argmin(&bestv);
+    if (crank == 0) {                                   // walk back to original step T-1
+      const uint32_t s = walk(bs, T - 1, T - 1 - rho, false);
+      if (tid == 0)
+        for (uint32_t c = 0; c < kCluster; ++c) st_peer(peer_addr(slots_sa + 32, c), s >> K);
     }
-    __syncthreads();
-    const uint32_t w = sh_u[0];
+    cluster_sync();
+    const uint32_t w = *slot_w;                         // the pre-window bits
 
-    // pass 2: constrained to w
-    float* c2 = (fin == cur) ? nxt : cur;
-    float* n2 = fin;
-    for (uint32_t s = tid; s < kStates; s += kEncThreads) c2[s] = INFINITY;
+    // pass 2: constrained to w, starting at step 0
+    build_costs(ct, lut, z, 0);
+    build_costs(ct + kCostBytes / 4, lut, z, 1);
     __syncthreads();
-    if (tid < (1u << K)) {
-      const uint32_t s = w | (tid << W);
-      c2[s] = branch_cost(lut, z, 0, s);
-    }
-    __syncthreads();
-    fin = viterbi_pass<K>(lut, z, T, Lc, c2, n2, tb, 0, static_cast<int64_t>(w));
-    bs = cta_argmin(fin, red_v, red_s, &bestv);
+    start_costs();
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q)
+      if (((base + q) & kMask) != w) v[q] = INFINITY;
+    for (uint32_t i = 1; i < T; ++i) step(i, i, i + 1, i + 1 < T, true, w);
+    bs = argmin(&bestv);
 
     // traceback: new bits of step t are the top K bits of s_t
-    for (uint32_t i = tid; i < code_bytes; i += kEncThreads) code[i] = 0;
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t s = bs;
-      for (int64_t t = T - 1; t >= 0; --t) {
-        const uint32_t x = s >> W;
-        for (uint32_t b = 0; b < K; ++b) {
-          const uint32_t j = K * static_cast<uint32_t>(t) + b;
-          if ((x >> b) & 1u) code[j >> 3] |= static_cast<uint8_t>(1u << (j & 7));
-        }
-        if (t > 0) {
-          const uint32_t g = s & (kGroups - 1);
-          s = (g << K) | tb[static_cast<size_t>(t) * kGroups + g];
-        }
+    if (crank == 0) {
+      for (uint32_t i = tid; i < code_bytes; i += kEncThreads) code[i] = 0;
+      __syncthreads();
+      const uint32_t s0 = walk(bs, T - 1, 0, true);     // state at step 0
+      if (tid == 0) {
+        const uint32_t x = s0 >> W;
+        for (uint32_t b = 0; b < K; ++b)
+          if ((x >> b) & 1u) code[b >> 3] |= static_cast<uint8_t>(1u << (b & 7));
       }
+    }
+    cluster_sync();                                     // traceback bytes free again
+    if (crank == 0) {
       // alpha = |e| / |f(c)|, |f|^2 in fp64 over coordinates in order
-      double fs = 0.0;
-      for (uint32_t t = 0; t < T; ++t) {
+      for (uint32_t t = tid; t < T; t += kEncThreads) {
         uint32_t st = 0;
         const int32_t first = static_cast<int32_t>(K * (t + 1)) - 16;
         for (int m = 0; m < 16; ++m) {
@@ -285,23 +492,25 @@ __global__ void __launch_bounds__(kEncThreads, 1) tcq_encode_kernel(const Encode
           if (pos < 0) pos += Lc;
           st |= static_cast<uint32_t>((code[pos >> 3] >> (pos & 7)) & 1u) << m;
         }
-        const float2 y = state_y(lut, st);
+        const float2 y = entry_y(lut, state_entry(st));
         const double y0 = y.x, y1 = y.y;
-        fs = __dadd_rn(fs, __dmul_rn(y0, y0));
-        fs = __dadd_rn(fs, __dmul_rn(y1, y1));
+        scratch[2 * t] = __dmul_rn(y0, y0);
+        scratch[2 * t + 1] = __dmul_rn(y1, y1);
       }
-      const uint16_t ab = double_to_bf16_rne(__ddiv_rn(nrm, __dsqrt_rn(fs)));
-      sh_u[1] = ab;
-      if (p.cost) p.cost[r] = bestv;
+      __syncthreads();
+      if (tid == 0) {
+        double fs = 0.0;
+        for (uint32_t q = 0; q < 2 * T; ++q) fs = __dadd_rn(fs, scratch[q]);
+        const uint16_t ab = double_to_bf16_rne(__ddiv_rn(nrm, __dsqrt_rn(fs)));
+        rec[code_bytes] = static_cast<uint8_t>(ab & 0xFF);
+        rec[code_bytes + 1] = static_cast<uint8_t>(ab >> 8);
+        if (p.cost) p.cost[r] = bestv;
+      }
+      for (uint32_t i = tid; i < code_bytes; i += kEncThreads) rec[i] = code[i];
+      __syncthreads();
     }
-    __syncthreads();
-    for (uint32_t i = tid; i < code_bytes; i += kEncThreads) rec[i] = code[i];
-    if (tid == 0) {
-      rec[code_bytes] = static_cast<uint8_t>(sh_u[1] & 0xFF);
-      rec[code_bytes + 1] = static_cast<uint8_t>(sh_u[1] >> 8);
-    }
-    __syncthreads();
   }
+  cluster_sync();                                       // no CTA leaves while peers may write to it
 }
 
 using EncodeFn = void (*)(EncodeParams);
@@ -334,21 +543,43 @@ extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
       return CP_ERR_FORMAT;
     }
   }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const uint32_t k = bits_per_step, T = d / 2, W = 16 - k;
-  const uint64_t ctas = rows < static_cast<uint64_t>(sms) ? rows : static_cast<uint64_t>(sms);
-  const uint64_t stride = ((2ull * cpk::kStates * sizeof(float) +
-                            static_cast<uint64_t>(T) * (1ull << W)) + 255) & ~255ull;
+  const cpk::EncSmem L = cpk::enc_smem(d, k);
+  cpk::EncodeFn fn = cpk::encode_kernel(k);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L.total));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cpk::kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(cpk::kEncThreads);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = 0;
+  if (err == cudaSuccess) {
+    cfg.gridDim = dim3(cpk::kCluster * 64);
+    err = cudaOccupancyMaxActiveClusters(&max_clusters, reinterpret_cast<const void*>(fn), &cfg);
+  }
+  if (err != cudaSuccess || max_clusters < 1) {
+    if (err == cudaSuccess) err = cudaErrorInvalidConfiguration;
+    return cpx::cuda_fail(err, "tcq encoder cluster occupancy");
+  }
+  const uint64_t clusters =
+      rows < static_cast<uint64_t>(max_clusters) ? rows : static_cast<uint64_t>(max_clusters);
+  const uint64_t stride = (static_cast<uint64_t>(T) * (1ull << W) + 255) & ~255ull;
   void* mem = nullptr;
-  cudaError_t err = cudaMalloc(&mem, ctas * stride + 2048);
+  err = cudaMalloc(&mem, clusters * stride + 2048);
   if (err != cudaSuccess) {
     cpx::cuda_fail(err, "cudaMalloc(encoder workspace)");
     return CP_ERR_NO_MEMORY;
   }
-  uint32_t* lut_dev = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mem) + ctas * stride);
+  uint32_t* lut_dev = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mem) + clusters * stride);
   err = cudaMemcpyAsync(lut_dev, lut_fp16, 2048, cudaMemcpyHostToDevice, s);
   cpk::EncodeParams p;
   p.e = e;
@@ -359,15 +590,9 @@ extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
   p.cost = cost;
   p.work = static_cast<uint8_t*>(mem);
   p.work_stride = stride;
-  const size_t smem = 2048 + 304 + 4ull * d + (k * T) / 8 + 16;
-  cpk::EncodeFn fn = cpk::encode_kernel(k);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err == cudaSuccess) {
-    void* args[] = {&p};
-    err = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(ctas)),
-                           dim3(cpk::kEncThreads), args, smem, s);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cpk::kCluster));
+    err = cudaLaunchKernelEx(&cfg, fn, p);
   }
   if (err == cudaSuccess) err = cudaStreamSynchronize(s);
   cudaFree(mem);

@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["encoder"], default=None,
+                    help="run one section alone (no table in device memory) and print its JSON")
+    ap.add_argument("--encoder-rows", type=int, default=0,
+                    help="rows per encoder call (default 4 x SM count)")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip timing the other table configs (mid, bit-rate sweep, decode step)")
     return ap.parse_args()
@@ -367,21 +371,8 @@ def our_arm(args, w, rank, world, local):
         mtable.close()
         del mbuf, moffs, ks, midx
 
-    # Offline compression on the GPU (the step before the hot path): 2 x SMs rows.
-    enc = None
-    if rank == 0 and w.d >= 16:
-        erows = 4 * torch.cuda.get_device_properties(0).multi_processor_count
-        e_in = torch.from_numpy(synth.normal_rows(synth.SEED_ENCODER_ROWS, erows, w.d)
-                                .astype(np.float32)).cuda()
-        cp.encode_rows(e_in[: erows // 2], w.k)                # warm-up
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        _, ecost = cp.encode_rows(e_in, w.k)
-        torch.cuda.synchronize()
-        et = time.perf_counter() - t0
-        enc = {"entry_point": "cp_encode_rows", "rows": erows, "seconds": et,
-               "rows_per_s": erows / et, "mean_cost_per_coord": float(ecost.mean()) / w.d}
-        del e_in
+    # Offline compression on the GPU (the step before the hot path).
+    enc = encoder_measure(args, w) if rank == 0 and w.d >= 16 else None
 
     # End to end through the public API: ids from pinned host memory, rows back
     # to pinned host memory, both copies inside the timed region.
@@ -456,6 +447,26 @@ def our_arm(args, w, rank, world, local):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def encoder_measure(args, w):
+    """cp_encode_rows on N(0,1) rows of the workload's d and rate: one warm-up call
+    on half the rows, then one timed call (host clock around call + sync)."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    erows = args.encoder_rows or 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    e_in = torch.from_numpy(synth.normal_rows(synth.SEED_ENCODER_ROWS, erows, w.d)
+                            .astype(np.float32)).cuda()
+    cp.encode_rows(e_in[: max(1, erows // 2)], w.k)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    _, ecost = cp.encode_rows(e_in, w.k)
+    torch.cuda.synchronize()
+    et = time.perf_counter() - t0
+    return {"entry_point": "cp_encode_rows", "rows": erows, "d": w.d, "b": w.k / 2,
+            "seconds": et, "rows_per_s": erows / et,
+            "mean_cost_per_coord": float(ecost.mean()) / w.d}
 
 
 OTHER_CONFIGS = ("mid", "sweep_b1.5", "sweep_b2", "sweep_b2.5", "sweep_b3", "deepseek_decode")
@@ -578,6 +589,12 @@ def main():
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
         reference_arm(args, w, rank)
+        return
+    if args.only == "encoder":
+        import torch
+        torch.cuda.set_device(local)
+        if rank == 0:
+            print(json.dumps({"encoder": encoder_measure(args, w)}), flush=True)
         return
     our_arm(args, w, rank, world, local)
 

@@ -217,8 +217,11 @@ cp_status cp_lookup_decode_reduce(const cp_table* t, const int64_t* idx, uint64_
  *   lut_fp16 host, 512 x (y0, y1) fp16 patterns (finite).
  *   records  device, rows * R bytes (R = d*k/16 + 2).
  *   cost     device fp32 [rows] (optional): the search's path metric.
- * Allocates and frees its workspace (about 0.5 MB + d/2 * 2^(16-k) bytes per SM)
- * and synchronises `stream` before returning.  d >= 16.
+ * Runs one 4-CTA thread-block cluster per row in flight.  Allocates and frees
+ * its workspace (d/2 * 2^(16-k) traceback bytes per cluster in flight, 2 MB at
+ * d = 1024, k = 4) and synchronises `stream` before returning.  d >= 16.
+ * Errors: CP_ERR_INVALID_ARG (pointers, geometry), CP_ERR_FORMAT (LUT),
+ * CP_ERR_NO_MEMORY (workspace), CP_ERR_CUDA (launch or cluster occupancy).
  */
 cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d, uint32_t bits_per_step,
                          const uint16_t* lut_fp16, uint8_t* records, float* cost, void* stream);

@@ -167,12 +167,13 @@ class ClockSampler:
 # Reference arm: the CPU oracle on the host cores.
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut):
-    """Oracle lookup-decode rows/s on a bounded prefix of the replay, all host cores."""
+def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut, threads: int = 0):
+    """Oracle lookup-decode rows/s on a bounded prefix of the replay (all host
+    cores unless `threads`)."""
     import torch
     import oracle
     from trellis_row_decode_gb300 import synth
-    nt = max(1, os.cpu_count() or 1)
+    nt = threads or max(1, os.cpu_count() or 1)
     # calibrate on a short prefix, then time a prefix sized for `seconds`
     def run(m):
         sub = idx[:m]
@@ -182,7 +183,7 @@ def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut):
         oracle.lookup_decode(rec, len(uniq), w.d, w.k, rec.shape[1], lut, inv.astype(np.int64),
                              n_threads=nt)
         return time.perf_counter() - t0
-    m0 = min(idx.size, 2048)
+    m0 = min(idx.size, 2048 if nt > 1 else 256)
     dt0 = run(m0)
     m = int(min(idx.size, max(m0, m0 * seconds / max(dt0, 1e-6))))
     dt = run(m)
@@ -380,10 +381,9 @@ def our_arm(args, w, rank, world, local):
     out_h = torch.empty((n, w.d), dtype=torch.bfloat16, pin_memory=True)
     idx_d = torch.empty_like(idx)
 
-    def e2e_step():
+    def e2e_step():                 # rows written by the kernel straight into pinned host memory
         idx_d.copy_(idx_h, non_blocking=True)
-        cp.lookup_decode(table, idx_d, out, stream)
-        out_h.copy_(out, non_blocking=True)
+        cp.lookup_decode(table, idx_d, out_h, stream)
 
     te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream)
     e2e_value = n / float(te.mean())
@@ -399,9 +399,12 @@ def our_arm(args, w, rank, world, local):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, m, nt = oracle_sample_rate(w, idx_np, args.cpu_seconds, cp.default_lut())
+        rate1, m1, _ = oracle_sample_rate(w, idx_np, args.cpu_seconds / 4, cp.default_lut(), 1)
         cpu = {"value": rate, "unit": "rows/s", "cores": nt, "kind": "oracle",
                "sample": f"first {m} lookups of the replay, records regenerated on the host, "
-                         f"{nt} threads"}
+                         f"{nt} threads",
+               "single_thread": {"value": rate1, "unit": "rows/s", "cores": 1,
+                                 "sample": f"first {m1} lookups of the replay"}}
 
     if rank == 0:
         clk = clocks.summary()
@@ -425,6 +428,7 @@ def our_arm(args, w, rank, world, local):
                          "traffic": ncu_traffic(w.name, args.layout),
                          "bytes_per_lookup": bpl, "kernel": "lookup_decode_kernel"},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": n * 8,
+                    "path": "ids copied from pinned host memory; rows written by the decode kernel into pinned host memory",
                     "d2h_bytes_per_step": n * w.d * 2},
             "gpu_launches": args.steps,
             "clocks": clk,

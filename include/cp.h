@@ -136,6 +136,10 @@ cp_status cp_table_load_mixed(cp_table** out, const void* records, const uint64_
  *
  *   idx   device pointer, n int64 row ids, 8-byte aligned.
  *   out   device pointer, bf16 [n][d] row-major (n*d*2 bytes), 16-byte aligned.
+ *         It may also be page-locked host memory that the device can address
+ *         (cudaHostAlloc, or cudaHostRegister with mapping; with unified
+ *         addressing the host pointer is the device pointer): the kernel then
+ *         writes the rows over the host link, with no separate copy.
  * Out-of-range ids give zero rows and set the status word (see cp_get_status).
  */
 cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,

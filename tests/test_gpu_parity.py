@@ -190,6 +190,20 @@ def test_non_default_stream(lut):
     _assert_exact(bits(out).reshape(-1, d), oracle_decode(SEED, d, k, idx_np, n_rows, lut))
 
 
+def test_output_in_pinned_host_memory(lut):
+    """cp_lookup_decode writing straight into page-locked host memory (over the
+    host link) gives the oracle's rows, including a ragged tail and bad ids."""
+    d, k, n_rows = 1024, 4, 3000
+    table = cp.load_table(device_table(SEED, n_rows, d, k), n_rows, d, k, lut)
+    idx_np = synth.uniform_indices(11, 4099, n_rows)
+    idx_np[7] = n_rows                                  # out of range -> zero row
+    out_h = torch.empty((idx_np.size, d), dtype=torch.bfloat16, pin_memory=True)
+    cp.lookup_decode(table, torch.from_numpy(idx_np).cuda(), out_h)
+    torch.cuda.synchronize()
+    _assert_exact(bits(out_h).reshape(-1, d), oracle_decode(SEED, d, k, idx_np, n_rows, lut))
+    assert cp.get_status(table) == cp.CP_ERR_INDEX_OOB
+
+
 def test_injected_failures(lut):
     d, k, n_rows = 256, 4, 16
     rec = device_table(SEED, n_rows, d, k)

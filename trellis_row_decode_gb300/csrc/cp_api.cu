@@ -172,7 +172,8 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     const bool cached = t->cache != nullptr && t->cmap_ts != 0;
     cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, cached ? t->cmap_keys : nullptr,
                        cached ? t->cmap_vals : nullptr, cached ? t->cmap_ts : 0,
-                       cached ? hs->cslot : nullptr, t->sm_count, stream);
+                       cached ? hs->cslot : nullptr, t->bucket_shift, t->bucket_nb, counts,
+                       t->sm_count, stream);
     cpk::launch_bucket_partition(idx + c0, dup, m, t->n_rows, t->bucket_shift, t->bucket_nb,
                                  counts, perm, t->sm_count, stream);
     cpk::DecodeParams pc = p;

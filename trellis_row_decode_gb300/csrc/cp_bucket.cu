@@ -50,12 +50,18 @@ __device__ __forceinline__ uint32_t slot_hash(unsigned long long key, uint32_t t
 
 // With a hot-row cache (cmap_ts > 0) the group's lowest lane also looks the id
 // up in the cache map (keys r + 1 -> slot) and the group writes cslot[j].
+// The same pass counts the lookups that will be visited (owners, and ids out of
+// range) per row-range bucket: counts[b] += (a shared-memory histogram per CTA).
 __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint64_t n_rows,
                               unsigned long long* __restrict__ keys, uint32_t* __restrict__ owner,
                               uint32_t ts, uint32_t* __restrict__ dup,
                               const unsigned long long* __restrict__ cmap_keys,
                               const uint32_t* __restrict__ cmap_vals, uint32_t cmap_ts,
-                              uint32_t* __restrict__ cslot) {
+                              uint32_t* __restrict__ cslot, uint32_t shift, uint32_t nb,
+                              uint32_t* __restrict__ counts) {
+  extern __shared__ uint32_t hist[];                    // nb + 1 bins
+  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
@@ -66,6 +72,7 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
     if (j < n && !valid) {
       dup[j] = kNoOwner;
       if (cmap_ts != 0) cslot[j] = kNoOwner;
+      atomicAdd(&hist[nb], 1u);
     }
     const uint32_t active = __ballot_sync(0xffffffffu, valid);
     if (!valid) continue;
@@ -108,8 +115,12 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
     }
     o = __shfl_sync(group, o, leader);
     dup[j] = o;
+    if (o == static_cast<uint32_t>(j)) atomicAdd(&hist[bucket_of(r, n_rows, shift, nb)], 1u);
     if (cmap_ts != 0) cslot[j] = __shfl_sync(group, cs, leader);
   }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x)
+    if (hist[i]) atomicAdd(&counts[i], hist[i]);
 }
 
 // Cache construction: warp per hot row, 2-byte granules (records are 2-byte
@@ -145,34 +156,39 @@ __global__ void cache_map_kernel(const int64_t* __restrict__ rows, uint64_t m,
   }
 }
 
-// Non-owner lookups copy their owner's decoded row (warp per row).
+// Non-owner lookups copy their owner's decoded row.  A warp reads 32 owner
+// entries at once and copies the rows of the non-owners among them one after
+// another, each lane loading its (up to) four 16-byte pieces before storing.
 __global__ void copy_dups_kernel(const uint32_t* __restrict__ dup, uint64_t n, uint32_t row16,
                                  uint4* __restrict__ out) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       j < n; j += warps) {
-    const uint32_t o = dup[j];
-    if (o == kNoOwner || o == static_cast<uint32_t>(j)) continue;
-    const uint4* src = out + static_cast<uint64_t>(o) * row16;
-    uint4* dst = out + j * row16;
-    for (uint32_t c = lane; c < row16; c += 32) __stcs(dst + c, __ldcg(src + c));
+  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
+       base < n; base += warps * 32) {
+    const uint64_t j = base + lane;
+    const uint32_t o = (j < n) ? __ldg(dup + j) : kNoOwner;
+    uint32_t todo = __ballot_sync(0xffffffffu, o != kNoOwner && o != static_cast<uint32_t>(j));
+    while (todo) {
+      const uint32_t l = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const uint32_t src_row = __shfl_sync(0xffffffffu, o, l);
+      const uint4* src = out + static_cast<uint64_t>(src_row) * row16;
+      uint4* dst = out + (base + l) * row16;
+      for (uint32_t c0 = 0; c0 < row16; c0 += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t c = c0 + 32 * u + lane;
+          if (c < row16) v[u] = __ldcg(src + c);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t c = c0 + 32 * u + lane;
+          if (c < row16) __stcs(dst + c, v[u]);
+        }
+      }
+    }
   }
-}
-
-// counts[b] += number of lookups in bucket b (shared-memory histogram per CTA).
-__global__ void bucket_count_kernel(const int64_t* __restrict__ idx, const uint32_t* __restrict__ dup,
-                                    uint64_t n, uint64_t n_rows, uint32_t shift, uint32_t nb,
-                                    uint32_t* __restrict__ counts) {
-  extern __shared__ uint32_t hist[];                    // nb + 1 bins
-  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const uint64_t lo = blockIdx.x * n / gridDim.x, hi = (blockIdx.x + 1) * n / gridDim.x;
-  for (uint64_t j = lo + threadIdx.x; j < hi; j += blockDim.x)
-    if (visits(dup, j)) atomicAdd(&hist[bucket_of(__ldg(idx + j), n_rows, shift, nb)], 1u);
-  __syncthreads();
-  for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x)
-    if (hist[i]) atomicAdd(&counts[i], hist[i]);
 }
 
 // In-place exclusive prefix sum of len words, one CTA of 1024 threads.
@@ -238,9 +254,11 @@ __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, const uin
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
                    uint32_t* owner, uint32_t ts, uint32_t* dup,
                    const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
-                   uint32_t cmap_ts, uint32_t* cslot, int sm_count, cudaStream_t s) {
-  dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(
-      idx, n, n_rows, keys, owner, ts, dup, cmap_keys, cmap_vals, cmap_ts, cslot);
+                   uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,
+                   uint32_t* counts, int sm_count, cudaStream_t s) {
+  dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, (nb + 1) * sizeof(uint32_t), s>>>(
+      idx, n, n_rows, keys, owner, ts, dup, cmap_keys, cmap_vals, cmap_ts, cslot, shift, nb,
+      counts);
 }
 
 void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, uint64_t m,
@@ -254,8 +272,6 @@ void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n
                              uint32_t shift, uint32_t nb, uint32_t* counts, uint32_t* perm,
                              int sm_count, cudaStream_t s) {
   const unsigned blocks = static_cast<unsigned>(sm_count);
-  bucket_count_kernel<<<blocks, 512, (nb + 1) * sizeof(uint32_t), s>>>(idx, dup, n, n_rows, shift,
-                                                                       nb, counts);
   bucket_scan_kernel<<<1, 1024, 0, s>>>(counts, nb + 1);
   bucket_scatter_kernel<<<blocks, 512, 0, s>>>(idx, dup, n, n_rows, shift, nb, counts, perm);
 }

@@ -67,10 +67,13 @@ constexpr uint32_t kHashSlotsMax = 2 * kBucketChunk;  // dedupe table slots (loa
 // are the open-addressing table, ts a power of two >= 2n.
 // With a hot-row cache map (cmap_ts > 0), also cslot[j] = cache slot of idx[j]
 // (or 0xFFFFFFFF when the id is not cached).
+// counts (nb + 1 words, zeroed by the caller) receives the number of lookups to
+// visit per bucket (id >> shift): the owners, and in bucket nb the ids out of range.
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
                    uint32_t* owner, uint32_t ts, uint32_t* dup,
                    const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
-                   uint32_t cmap_ts, uint32_t* cslot, int sm_count, cudaStream_t s);
+                   uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,
+                   uint32_t* counts, int sm_count, cudaStream_t s);
 
 // Hot-row cache construction: records of the m rows `rows` (device ids, sorted)
 // copied from the host table alias into `cache` (stride R), and the map
@@ -79,9 +82,9 @@ void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, u
                         uint8_t* cache, unsigned long long* keys, uint32_t* vals, uint32_t ts,
                         int sm_count, cudaStream_t s);
 
-// Partition of the lookups that own their id (all of them if dup is null) by
-// (id >> shift), ids outside [0, n_rows) in the last bucket.  counts: nb + 1
-// words, zeroed by the caller; afterwards counts[nb] = number of visits.
+// Partition of the lookups that own their id by (id >> shift), ids outside
+// [0, n_rows) in the last bucket.  counts: the nb + 1 per-bucket visit counts
+// from launch_dedupe; afterwards counts[nb] = number of visits.
 void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,
                              uint32_t shift, uint32_t nb, uint32_t* counts, uint32_t* perm,
                              int sm_count, cudaStream_t s);

@@ -513,6 +513,20 @@ def other_configs(args, w, table, idx, out, flush, stream):
         del rec, oidx, oout
         torch.cuda.empty_cache()
 
+    # the SoA layout (codes and scales in separate arrays) on the 2^24-row b = 2 table
+    ow = synth.WORKLOADS["sweep_b2"]
+    if ow.table_bytes <= (16 << 30):
+        tab, rec, soa = build_table(ow, "soa", synth.SEED_TABLE)
+        oidx = torch.from_numpy(ow.indices()).cuda()
+        oout = torch.empty((oidx.numel(), ow.d), dtype=torch.bfloat16, device="cuda")
+        t = time_steps(lambda: cp.lookup_decode(tab, oidx, oout, stream), steps, args.warmup,
+                       flush, stream)
+        assert cp.get_status(tab) == cp.CP_OK
+        res["sweep_b2 (SoA layout)"] = entry(ow, oidx.numel(), float(np.median(t)))
+        tab.close()
+        del rec, soa, oidx, oout
+        torch.cuda.empty_cache()
+
     # the same replay as two calls, one per layer of 24 rows per token
     if w.rows_per_token == 48:
         lay = idx.view(w.tokens, 2, 24)

@@ -48,8 +48,10 @@ __device__ __forceinline__ uint32_t slot_hash(unsigned long long key, uint32_t t
   return static_cast<uint32_t>((key * 0x9E3779B97F4A7C15ull) >> 32) & (ts - 1);
 }
 
-// With a hot-row cache (cmap_ts > 0) the group's lowest lane also looks the id
-// up in the cache map (keys r + 1 -> slot) and the group writes cslot[j].
+// With a hot-row cache (cmap_ts > 0) the group's lowest lane first looks the id
+// up in the cache map (keys r + 1 -> slot) and the group writes cslot[j]; a
+// cached id skips the owner table (every one of its lookups owns itself and is
+// decoded from the HBM copy, so no row is copied afterwards).
 // The same pass counts the lookups that will be visited (owners, and ids out of
 // range) per row-range bucket: counts[b] += (a shared-memory histogram per CTA).
 __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint64_t n_rows,
@@ -93,7 +95,9 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
         slot = (slot + 1) & (cmap_ts - 1);
       }
     }
-    if (lane == leader) {
+    // a cached id needs no owner: each of its lookups decodes from the HBM copy
+    cs = __shfl_sync(group, cs, leader);
+    if (lane == leader && cs == kNoOwner) {
       uint32_t slot = slot_hash(key, ts);
       for (uint32_t probe = 0; probe < ts; ++probe) {
         unsigned long long cur = __ldcg(keys + slot);
@@ -113,10 +117,10 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
         slot = (slot + 1) & (ts - 1);
       }
     }
-    o = __shfl_sync(group, o, leader);
+    o = (cs == kNoOwner) ? __shfl_sync(group, o, leader) : static_cast<uint32_t>(j);
     dup[j] = o;
     if (o == static_cast<uint32_t>(j)) atomicAdd(&hist[bucket_of(r, n_rows, shift, nb)], 1u);
-    if (cmap_ts != 0) cslot[j] = __shfl_sync(group, cs, leader);
+    if (cmap_ts != 0) cslot[j] = cs;
   }
   __syncthreads();
   for (uint32_t i = threadIdx.x; i <= nb; i += blockDim.x)

@@ -164,11 +164,6 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     const uint64_t m = (n - c0 < cap) ? n - c0 : cap;
     uint32_t ts = 1024;
     while (ts < 2 * m) ts <<= 1;
-    e = cudaMemsetAsync(keys, 0, ts * sizeof(unsigned long long), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(owner, 0xFF, ts * sizeof(uint32_t), stream);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(counts, 0, (t->bucket_nb + 1) * sizeof(uint32_t), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "scratch reset");
     const bool cached = t->cache != nullptr && t->cmap_ts != 0;
     cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, cached ? t->cmap_keys : nullptr,
                        cached ? t->cmap_vals : nullptr, cached ? t->cmap_ts : 0,

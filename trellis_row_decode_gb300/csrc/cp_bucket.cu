@@ -195,6 +195,18 @@ __global__ void copy_dups_kernel(const uint32_t* __restrict__ dup, uint64_t n, u
   }
 }
 
+// Start of a pass: empty owner table (keys 0, owners 0xFFFFFFFF) of ts slots
+// and zero bucket counts.
+__global__ void reset_kernel(unsigned long long* __restrict__ keys, uint32_t* __restrict__ owner,
+                             uint32_t ts, uint32_t* __restrict__ counts, uint32_t n_counts) {
+  const uint32_t T = gridDim.x * blockDim.x;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < ts; i += T) {
+    keys[i] = 0ull;
+    owner[i] = kNoOwner;
+  }
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counts; i += T) counts[i] = 0;
+}
+
 // In-place exclusive prefix sum of len words, one CTA of 1024 threads.
 __global__ void bucket_scan_kernel(uint32_t* __restrict__ counts, uint32_t len) {
   __shared__ uint32_t warp_sum[32];
@@ -260,6 +272,8 @@ void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned lon
                    const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
                    uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,
                    uint32_t* counts, int sm_count, cudaStream_t s) {
+  reset_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, 0, s>>>(keys, owner, ts, counts,
+                                                                  nb + 1);
   dedupe_kernel<<<static_cast<unsigned>(sm_count) * 2, 512, (nb + 1) * sizeof(uint32_t), s>>>(
       idx, n, n_rows, keys, owner, ts, dup, cmap_keys, cmap_vals, cmap_ts, cslot, shift, nb,
       counts);

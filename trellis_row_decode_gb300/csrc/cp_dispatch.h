@@ -63,12 +63,13 @@ constexpr uint32_t kBucketChunk = 1u << 20;           // lookups per pass
 constexpr uint32_t kHashSlotsMax = 2 * kBucketChunk;  // dedupe table slots (load <= 1/2)
 
 // dup[j] = owner lookup of idx[j] among n lookups (kNoOwner for ids outside
-// [0, n_rows)); keys (ts 64-bit words, zeroed) and owner (ts words, 0xFF-filled)
-// are the open-addressing table, ts a power of two >= 2n.
+// [0, n_rows)); keys (ts 64-bit words) and owner (ts words) are the
+// open-addressing table, ts a power of two >= 2n, emptied by a reset kernel that
+// this call queues first.
 // With a hot-row cache map (cmap_ts > 0), also cslot[j] = cache slot of idx[j]
 // (or 0xFFFFFFFF when the id is not cached).
-// counts (nb + 1 words, zeroed by the caller) receives the number of lookups to
-// visit per bucket (id >> shift): the owners, and in bucket nb the ids out of range.
+// counts (nb + 1 words, zeroed by the same reset) receives the number of lookups
+// to visit per bucket (id >> shift): the owners, and in bucket nb the ids out of range.
 void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
                    uint32_t* owner, uint32_t ts, uint32_t* dup,
                    const unsigned long long* cmap_keys, const uint32_t* cmap_vals,

@@ -165,8 +165,9 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     uint32_t ts = 1024;
     while (ts < 2 * m) ts <<= 1;
     const bool cached = t->cache != nullptr && t->cmap_ts != 0;
-    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup, cached ? t->cmap_keys : nullptr,
-                       cached ? t->cmap_vals : nullptr, cached ? t->cmap_ts : 0,
+    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup,
+                       cached ? t->cmap_keys : nullptr, cached ? t->cmap_vals : nullptr,
+                       cached ? t->cmap_ts : 0,
                        cached ? hs->cslot : nullptr, t->bucket_shift, t->bucket_nb, counts,
                        t->sm_count, stream);
     cpk::launch_bucket_partition(idx + c0, dup, m, t->n_rows, t->bucket_shift, t->bucket_nb,
@@ -227,7 +228,8 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
   const int pf = cpk::kPfDevice;
   int nwarps = cpk::kMaxWarps;
   auto smem_for = [&](int w) {
-    return static_cast<size_t>(cpk::lut_bytes(32)) + static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
+    return static_cast<size_t>(cpk::lut_bytes(32)) +
+           static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
   };
   while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
   const size_t smem = smem_for(nwarps);
@@ -577,7 +579,8 @@ cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, v
   if (t == nullptr) return CP_ERR_INVALID_ARG;
   if (t->residency != CP_RESIDENT_HOST || t->layout != CP_LAYOUT_AOS ||
       !cpk::host_uses_register_ring(cpk::cpl_index(t->d))) {
-    cpx::set_error("the hot-row cache applies to host-resident AoS tables with d = 256, 512 or 1024");
+    cpx::set_error(
+        "the hot-row cache applies to host-resident AoS tables with d = 256, 512 or 1024");
     return CP_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -600,7 +603,8 @@ cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, v
   std::vector<int64_t> rows(hot_rows, hot_rows + m);
   std::sort(rows.begin(), rows.end());            // ascending: link-friendly copy order
   for (uint64_t i = 0; i < m; ++i) {
-    if (rows[i] < 0 || static_cast<uint64_t>(rows[i]) >= t->n_rows || (i > 0 && rows[i] == rows[i - 1])) {
+    if (rows[i] < 0 || static_cast<uint64_t>(rows[i]) >= t->n_rows ||
+        (i > 0 && rows[i] == rows[i - 1])) {
       cpx::set_error("hot rows must be distinct ids in [0, n_rows)");
       return CP_ERR_INVALID_ARG;
     }
@@ -629,8 +633,8 @@ cp_status cp_table_set_cache(cp_table* t, const int64_t* hot_rows, uint64_t m, v
     cudaFree(mem);
     return cuda_fail(e, "cache map upload");
   }
-  cpk::launch_cache_build(t->rec, t->rec_bytes, rows_dev, m, static_cast<uint8_t*>(cache), keys, vals,
-                          ts, t->sm_count, s);
+  cpk::launch_cache_build(t->rec, t->rec_bytes, rows_dev, m, static_cast<uint8_t*>(cache), keys,
+                          vals, ts, t->sm_count, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFree(mem);

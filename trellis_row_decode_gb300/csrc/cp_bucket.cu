@@ -26,8 +26,13 @@ constexpr uint32_t kNoOwner = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint32_t bucket_of(int64_t r, uint64_t n_rows, uint32_t shift,
                                               uint32_t nb) {
-  return (static_cast<uint64_t>(r) < n_rows) ? static_cast<uint32_t>(static_cast<uint64_t>(r) >> shift)
-                                             : nb;
+  const uint64_t u = static_cast<uint64_t>(r);
+  return (u < n_rows) ? static_cast<uint32_t>(u >> shift) : nb;
+}
+
+// First lookup of this warp's first batch of 32 (grid-stride over batches).
+__device__ __forceinline__ uint64_t warp_batch0() {
+  return (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
 }
 
 // Lookup j takes part in the partition when it owns its id, or its id is out
@@ -66,8 +71,7 @@ __global__ void dedupe_kernel(const int64_t* __restrict__ idx, uint64_t n, uint6
   __syncthreads();
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
-       base < n; base += warps * 32) {
+  for (uint64_t base = warp_batch0(); base < n; base += warps * 32) {
     const uint64_t j = base + lane;
     const int64_t r = (j < n) ? __ldg(idx + j) : -1;
     const bool valid = j < n && static_cast<uint64_t>(r) < n_rows;
@@ -136,7 +140,8 @@ __global__ void cache_fill_kernel(const uint8_t* __restrict__ table, uint32_t R,
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   for (uint64_t s = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        s < m; s += warps) {
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(table + static_cast<uint64_t>(rows[s]) * R);
+    const uint16_t* src =
+        reinterpret_cast<const uint16_t*>(table + static_cast<uint64_t>(rows[s]) * R);
     uint16_t* dst = reinterpret_cast<uint16_t*>(cache + s * R);
     for (uint32_t i = lane; i < R / 2; i += 32) dst[i] = src[i];
   }
@@ -167,8 +172,7 @@ __global__ void copy_dups_kernel(const uint32_t* __restrict__ dup, uint64_t n, u
                                  uint4* __restrict__ out) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
-       base < n; base += warps * 32) {
+  for (uint64_t base = warp_batch0(); base < n; base += warps * 32) {
     const uint64_t j = base + lane;
     const uint32_t o = (j < n) ? __ldg(dup + j) : kNoOwner;
     uint32_t todo = __ballot_sync(0xffffffffu, o != kNoOwner && o != static_cast<uint32_t>(j));
@@ -242,13 +246,13 @@ __global__ void bucket_scan_kernel(uint32_t* __restrict__ counts, uint32_t len) 
 }
 
 // perm[cursor[b]++] = j, one atomic per (warp, bucket) group.
-__global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, const uint32_t* __restrict__ dup,
+__global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx,
+                                      const uint32_t* __restrict__ dup,
                                       uint64_t n, uint64_t n_rows, uint32_t shift, uint32_t nb,
                                       uint32_t* __restrict__ cursor, uint32_t* __restrict__ perm) {
   const uint32_t lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (uint64_t base = (static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
-       base < n; base += warps * 32) {
+  for (uint64_t base = warp_batch0(); base < n; base += warps * 32) {
     const uint64_t j = base + lane;
     const bool valid = j < n && visits(dup, j);
     const uint32_t active = __ballot_sync(0xffffffffu, valid);

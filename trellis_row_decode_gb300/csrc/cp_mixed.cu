@@ -10,7 +10,8 @@ namespace cpk {
 __global__ void check_mixed_offsets_kernel(const uint64_t* __restrict__ offsets, uint64_t n_rows,
                                            uint32_t d, uint32_t* __restrict__ bad) {
   const uint64_t T = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t r = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < n_rows; r += T) {
+  for (uint64_t r = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < n_rows;
+       r += T) {
     const uint64_t o0 = offsets[r], o1 = offsets[r + 1];
     bool ok = o1 > o0 && (o0 & 1) == 0 && (r != 0 || o0 == 0);
     if (ok) {

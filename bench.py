@@ -99,6 +99,30 @@ def kernel_source_sha() -> str:
     return h.hexdigest()
 
 
+ISSUE_PEAK_WARP_INST_S = 152 * 4 * 2.07e9   # SMs x schedulers x 1 warp-instruction/clock x max SM clock
+
+
+def header_sha(name: str) -> str:
+    h = hashlib.sha256()
+    f = ROOT / "trellis_row_decode_gb300" / "csrc" / name
+    h.update(f.name.encode())
+    h.update(f.read_bytes())
+    return h.hexdigest()
+
+
+def ncu_inst(kernel: str, n: int, d: int, k: int, group: int):
+    """Committed warp-instruction count per launch, or None (header changed / no entry)."""
+    try:
+        data = json.loads((ROOT / "profiles" / "ncu_inst.json").read_text())
+    except (OSError, ValueError):
+        return None
+    for e in data.get("entries", []):
+        if (e.get("kernel"), e.get("n"), e.get("d"), e.get("k"), e.get("group")) == \
+                (kernel, n, d, k, group) and e.get("header_sha256") == header_sha(e["header"]):
+            return int(e["warp_instructions"])
+    return None
+
+
 def ncu_traffic(workload: str, layout: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
     p = ROOT / "profiles" / "ncu_traffic.json"
@@ -345,6 +369,13 @@ def our_arm(args, w, rank, world, local):
                  "ms_per_step": tm * 1e3, "lookups_per_s": n / tm,
                  "algorithmic_gbs": fbytes / tm / 1e9, "bytes_per_step": fbytes,
                  "frac_of_hbm_peak": fbytes / tm / 1e9 / measured_peaks()[0]}
+        inst = ncu_inst("lookup_decode_reduce_kernel", n, w.d, w.k, group)
+        if inst is not None:
+            fused["roofline"] = {"bound": "alu", "achieved": inst / tm,
+                                 "peak": ISSUE_PEAK_WARP_INST_S, "unit": "warp-inst/s",
+                                 "frac": inst / tm / ISSUE_PEAK_WARP_INST_S,
+                                 "peak_kind": "derived: 152 SMs x 4 schedulers x 2.07 GHz",
+                                 "inst_per_launch": inst}
         del red_out, gates
 
     # Mixed per-row bit rates (frequency-based allocation): 2^24 rows x the same d,

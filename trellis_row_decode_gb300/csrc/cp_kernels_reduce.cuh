@@ -20,16 +20,31 @@ namespace cpk {
 #endif
 constexpr int kReduceWarps = CP_REDUCE_WARPS;
 
+// acc (a pair of fp32 accumulators in one 64-bit register) += w2 * v, pairwise
+// (fma.rn.f32x2: each lane an fp32 fused multiply-add with one rounding, as fmaf).
+__device__ __forceinline__ void fma_pair(unsigned long long& acc, unsigned long long w2,
+                                         uint32_t lo_bits, uint32_t hi_bits) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo_bits), "r"(hi_bits));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w2), "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long pair_of(float x) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+
+// One chunk (8 coordinates): the bf16 row values, widened exactly, times the
+// lookup's weight, added to the four accumulator pairs.
 template <int K, bool F16, int REP>
 __device__ __forceinline__ void acc_chunk(uint64_t x, const uint8_t* lut, uint32_t lane4,
-                                          uint16_t a_h, float a, float wgt, float* acc) {
+                                          uint16_t a_h, float a, unsigned long long w2,
+                                          unsigned long long* acc) {
   const uint4 o = decode_chunk<K, F16, REP>(x, lut, lane4, a_h, a);
   const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    acc[2 * j] = __fmaf_rn(wgt, __uint_as_float(ow[j] << 16), acc[2 * j]);
-    acc[2 * j + 1] = __fmaf_rn(wgt, __uint_as_float(ow[j] & 0xFFFF0000u), acc[2 * j + 1]);
-  }
+  for (int j = 0; j < 4; ++j) fma_pair(acc[j], w2, ow[j] << 16, ow[j] & 0xFFFF0000u);
 }
 
 template <int K, bool SOA, int PF, int CPL>
@@ -123,11 +138,11 @@ __global__ void __launch_bounds__(kReduceWarps * 32, 1)
     else cp_async_commit();
   }
 
-  float acc[CPL][8];
+  unsigned long long acc[CPL][4];                       // fp32 pairs (coordinates 2j, 2j+1)
 #pragma unroll
   for (int m = 0; m < CPL; ++m)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[m][e] = 0.0f;
+    for (int e = 0; e < 4; ++e) acc[m][e] = 0ull;
   uint32_t in_group = 0;
   uint4* orow = reinterpret_cast<uint4*>(p.out) + g_lo * (d >> 3);
   const uint32_t lane4 = lane << 2;
@@ -140,7 +155,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32, 1)
     const uint32_t st = i & (PF - 1);
     uint8_t* sb = stages + st * stage_bytes + kStagePrefix;
     const uint32_t m = meta[2 * st];
-    const float wgt = __uint_as_float(meta[2 * st + 1]);
+    const unsigned long long wgt = pair_of(__uint_as_float(meta[2 * st + 1]));
     if (m & 1u) {
       const uint32_t mis = m >> 8;
       uint8_t* code = sb + mis;
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32, 1)
 #pragma unroll
       for (int c = 0; c < CPL; ++c)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(wgt, 0.0f, acc[c][e]);
+        for (int e = 0; e < 4; ++e) fma_pair(acc[c][e], wgt, 0u, 0u);   // w * (+0) added
     }
     __syncwarp();
     if (++in_group == group) {                            // group complete: one bf16 row
@@ -182,12 +197,14 @@ __global__ void __launch_bounds__(kReduceWarps * 32, 1)
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const __nv_bfloat162 r = __floats2bfloat162_rn(acc[c][2 * j], acc[c][2 * j + 1]);
+          float lo, hi;
+          asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc[c][j]));
+          const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
           o[j] = *reinterpret_cast<const uint32_t*>(&r);
         }
         __stcs(orow + lane + 32 * c, make_uint4(o[0], o[1], o[2], o[3]));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) acc[c][e] = 0ull;
       }
       orow += d >> 3;
       in_group = 0;

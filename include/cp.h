@@ -35,7 +35,12 @@
  *
  * Conventions for every call:
  *   - Stream-ordered and asynchronous on `stream` (a cudaStream_t; NULL = the
- *     legacy default stream).  No call synchronises except cp_get_status.
+ *     legacy default stream).  The decode calls (cp_lookup_decode,
+ *     cp_lookup_decode_host, cp_lookup_decode_reduce) queue kernels only: they
+ *     never synchronise or allocate, so they can be captured into a CUDA graph
+ *     and replayed (with new ids written into the captured buffers).  The calls
+ *     that synchronise `stream` say so: cp_get_status, cp_table_load_mixed,
+ *     cp_table_set_cache and cp_encode_rows.
  *   - Argument errors are detected on the host and returned before any work is
  *     queued; nothing is written in that case.
  *   - The caller owns every large buffer (records, SoA copy, ids, output); a

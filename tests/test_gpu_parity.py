@@ -339,3 +339,41 @@ def test_device_generator_matches_host():
     a = synth.gen_records(3, rows.cuda(), 1024, 5).cpu()
     b = synth.gen_records(3, rows, 1024, 5)
     assert torch.equal(a, b)
+
+
+def test_cuda_graph_capture_and_replay(lut):
+    """cp_lookup_decode and cp_lookup_decode_host queue only kernels (no host
+    synchronisation, no allocation), so both can be captured into a CUDA graph;
+    replays with new ids in the captured buffers give the oracle's rows."""
+    d, k, n_rows, n = 512, 4, 5000, 3000
+    rec = device_table(SEED, n_rows, d, k)
+    table = cp.load_table(rec, n_rows, d, k, lut)
+    host_rec = rec.cpu().pin_memory()
+    htable = cp.load_table(host_rec, n_rows, d, k, lut)
+    idx = torch.empty(n, dtype=torch.int64, device="cuda")
+    out = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    idx.copy_(torch.from_numpy(synth.uniform_indices(1, n, n_rows)))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):                          # first calls outside the capture
+        cp.lookup_decode(table, idx, out, s)
+        cp.lookup_decode_host(htable, idx, out_h, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cp.lookup_decode(table, idx, out, s)
+        cp.lookup_decode_host(htable, idx, out_h, s)
+    for seed in (21, 22):
+        idx_np = synth.uniform_indices(seed, n, n_rows)
+        idx.copy_(torch.from_numpy(idx_np))
+        out.zero_()
+        out_h.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle_decode(SEED, d, k, idx_np, n_rows, lut)
+        _assert_exact(bits(out).reshape(-1, d), ref, f"graph replay, seed {seed}")
+        _assert_exact(bits(out_h).reshape(-1, d), ref, f"graph replay (host table), seed {seed}")
+    assert cp.get_status(table) == cp.CP_OK and cp.get_status(htable) == cp.CP_OK
+    table.close()
+    htable.close()

@@ -23,7 +23,8 @@
 // memory, one cluster barrier per step.  The branch cost depends on the state
 // only through its signed LUT entry, so each step first tabulates the 1024
 // possible costs in shared memory (replicated against bank conflicts).  The
-// traceback bytes (one per group and step) go to a per-cluster global scratch.
+// traceback bytes (one per group and step) go to a per-cluster global scratch;
+// CTA 0 walks them back after each pass from chunks copied into shared memory.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>

@@ -45,6 +45,7 @@ FALLBACK_HBM_GBS = 6800.0       # earlier GB300 copy measurement, used when no m
 PAGES_LATENCY_S = 0.190e-3      # pages' HBM-resident replay latency on one H200
 L2_FLUSH_BYTES = 1024 << 20     # 512 MB written + 512 MB read between steps
 METRIC = "CP lookup-decode rows/s & achieved HBM GB/s, 4096-tok×48-row replay"
+REFERENCE_SECONDS = 60.0        # oracle time of a whole --impl reference run
 
 
 def parse():
@@ -191,27 +192,42 @@ class ClockSampler:
 # Reference arm: the CPU oracle on the host cores.
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut, threads: int = 0):
-    """Oracle lookup-decode rows/s on a bounded prefix of the replay (all host
-    cores unless `threads`)."""
+def oracle_runner(w, idx: np.ndarray, lut, threads: int = 0):
+    """run(m) -> seconds the oracle takes to decode the first m lookups of the
+    replay (records regenerated on the host first, outside the timing)."""
     import torch
     import oracle
     from trellis_row_decode_gb300 import synth
     nt = threads or max(1, os.cpu_count() or 1)
-    # calibrate on a short prefix, then time a prefix sized for `seconds`
+
+    cache = {}
+
     def run(m):
-        sub = idx[:m]
-        uniq, inv = np.unique(sub, return_inverse=True)
-        rec = synth.gen_records(synth.SEED_TABLE, torch.from_numpy(uniq), w.d, w.k).numpy()
+        if m not in cache:                       # records of the prefix, built once per m
+            uniq, inv = np.unique(idx[:m], return_inverse=True)
+            rec = synth.gen_records(synth.SEED_TABLE, torch.from_numpy(uniq), w.d, w.k).numpy()
+            cache.clear()
+            cache[m] = (rec, len(uniq), inv.astype(np.int64))
+        rec, nu, inv = cache[m]
         t0 = time.perf_counter()
-        oracle.lookup_decode(rec, len(uniq), w.d, w.k, rec.shape[1], lut, inv.astype(np.int64),
-                             n_threads=nt)
+        oracle.lookup_decode(rec, nu, w.d, w.k, rec.shape[1], lut, inv, n_threads=nt)
         return time.perf_counter() - t0
-    m0 = min(idx.size, 2048 if nt > 1 else 256)
+    return run, nt
+
+
+def oracle_sample_size(run, n: int, seconds: float, m0: int) -> int:
+    """Prefix length whose decode takes about `seconds` (calibrated on m0 lookups)."""
+    m0 = min(n, m0)
     dt0 = run(m0)
-    m = int(min(idx.size, max(m0, m0 * seconds / max(dt0, 1e-6))))
-    dt = run(m)
-    return m / dt, m, nt
+    return int(min(n, max(m0, m0 * seconds / max(dt0, 1e-6))))
+
+
+def oracle_sample_rate(w, idx: np.ndarray, seconds: float, lut, threads: int = 0):
+    """Oracle lookup-decode rows/s on a bounded prefix of the replay (all host
+    cores unless `threads`)."""
+    run, nt = oracle_runner(w, idx, lut, threads)
+    m = oracle_sample_size(run, idx.size, seconds, 2048 if nt > 1 else 256)
+    return m / run(m), m, nt
 
 
 def reference_arm(args, w, rank):
@@ -220,13 +236,19 @@ def reference_arm(args, w, rank):
     import trellis_row_decode_gb300 as cp
     lut = cp.default_lut()
     idx = w.indices()
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    per_step = min(per_step, 10.0)
-    rates, sizes, nt = [], [], 1
+    # the whole run stays near args.cpu_seconds: each step times a prefix sized
+    # for its share (at least the 2048-lookup calibration prefix)
+    # one calibration, then every step times the same prefix, sized so that the
+    # whole run takes about REFERENCE_SECONDS of oracle time
+    run, nt = oracle_runner(w, idx, lut)
+    per_step = REFERENCE_SECONDS / max(1, args.steps + args.warmup)
+    run(2048)                                    # first call: thread pool and pages warm
+    m = oracle_sample_size(run, idx.size, min(max(per_step, 0.002), 10.0), 2048)
+    rates, sizes = [], []
     for s in range(args.warmup + args.steps):
-        rate, m, nt = oracle_sample_rate(w, idx, per_step, lut)
+        dt = run(m)
         if s >= args.warmup:
-            rates.append(rate)
+            rates.append(m / dt)
             sizes.append(m)
     value = float(np.median(rates))
     bpl = w.algorithmic_bytes_per_lookup()
@@ -238,8 +260,8 @@ def reference_arm(args, w, rank):
         "config": {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
                    "lookups": w.n_lookups, "index_dist": f"{w.dist}({w.zipf_s})"},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nt, "kind": "oracle",
-                         "sample": f"first {sizes[0]} lookups of the replay per step, "
-                                   f"records regenerated on the host, {nt} threads"},
+                         "sample": f"first {sizes[0]} lookups of the replay per step (records "
+                                   f"regenerated on the host once), {nt} threads"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "achieved_gbs_algorithmic": value * bpl / 1e9,

@@ -194,7 +194,11 @@ def _decode(fn, table: Table, idx: torch.Tensor, out: torch.Tensor | None, strea
 
 def lookup_decode(table: Table, idx: torch.Tensor, out: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:
-    """bf16 [n, d] rows alpha_r * f(c_r) for r = idx[j], in lookup order (HBM-resident table)."""
+    """bf16 [n, d] rows alpha_r * f(c_r) for r = idx[j], in lookup order (HBM-resident table).
+
+    `out` may be a CUDA tensor or a pinned host tensor (the kernel then writes the
+    rows over the host link).  Only kernels are queued, so the call can be
+    captured into a CUDA graph."""
     return _decode(lib().cp_lookup_decode, table, idx, out, stream, "cp_lookup_decode")
 
 

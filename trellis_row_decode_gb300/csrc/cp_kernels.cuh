@@ -180,12 +180,15 @@ __device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uin
 }
 
 // Launch constants of the HBM-resident path: stages per warp (one row ahead)
-// and LUT replicas.
+// and LUT replicas.  16 replicas: a warp's LUT read takes about 1.5 shared
+// wavefronts (lanes l and l + 16 share a replica) instead of 1, which the
+// memory-bound decode does not notice, and the per-launch fill is half of 32
+// replicas' (64 KB per CTA instead of 128 KB).
 #ifndef CP_PF_DEVICE
 #define CP_PF_DEVICE 2
 #endif
 constexpr int kPfDevice = CP_PF_DEVICE;
-constexpr int kLutRepDevice = 32;
+constexpr int kLutRepDevice = 16;
 
 // Byte offset of the record data inside a stage (room for the spliced tail).
 constexpr uint32_t kStagePrefix = 16;
@@ -194,7 +197,7 @@ constexpr uint32_t kStagePrefix = 16;
 // CPL: chunks per lane when d == 256 * CPL, 0 for any d (runtime loop).
 // PERM: lookups are visited in the order p.perm (rows still land at their own
 // output position); used to give host-resident tables address locality.
-// REP: LUT replicas in shared memory (32 or 4).
+// REP: LUT replicas in shared memory (16 or 4).
 template <int K, bool SOA, int PF, int CPL, bool PERM, int REP>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];

@@ -124,6 +124,19 @@ def ncu_inst(kernel: str, n: int, d: int, k: int, group: int):
     return None
 
 
+def ncu_encoder_inst_per_row(d: int, k: int):
+    """Committed encoder warp instructions per row at (d, k), or None."""
+    try:
+        data = json.loads((ROOT / "profiles" / "ncu_inst.json").read_text())
+    except (OSError, ValueError):
+        return None
+    for e in data.get("entries", []):
+        if (e.get("kernel"), e.get("d"), e.get("k")) == ("tcq_encode_kernel", d, k) and \
+                e.get("header_sha256") == header_sha(e["header"]):
+            return float(e["warp_instructions_per_row"])
+    return None
+
+
 def ncu_traffic(workload: str, layout: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
     p = ROOT / "profiles" / "ncu_traffic.json"
@@ -521,9 +534,18 @@ def encoder_measure(args, w):
     _, ecost = cp.encode_rows(e_in, w.k)
     torch.cuda.synchronize()
     et = time.perf_counter() - t0
-    return {"entry_point": "cp_encode_rows", "rows": erows, "d": w.d, "b": w.k / 2,
-            "seconds": et, "rows_per_s": erows / et,
-            "mean_cost_per_coord": float(ecost.mean()) / w.d}
+    res = {"entry_point": "cp_encode_rows", "rows": erows, "d": w.d, "b": w.k / 2,
+           "seconds": et, "rows_per_s": erows / et,
+           "mean_cost_per_coord": float(ecost.mean()) / w.d}
+    ipr = ncu_encoder_inst_per_row(w.d, w.k)
+    if ipr is not None:
+        res["roofline"] = {"bound": "alu", "achieved": ipr * erows / et,
+                           "peak": ISSUE_PEAK_WARP_INST_S, "unit": "warp-inst/s",
+                           "frac": ipr * erows / et / ISSUE_PEAK_WARP_INST_S,
+                           "peak_kind": "derived: 152 SMs x 4 schedulers x 2.07 GHz",
+                           "inst_per_row": ipr,
+                           "note": "call time on the host clock (workspace allocation included)"}
+    return res
 
 
 OTHER_CONFIGS = ("mid", "sweep_b1.5", "sweep_b2", "sweep_b2.5", "sweep_b3", "deepseek_decode")

@@ -11,9 +11,12 @@ from L2 and no dirty flush lines are written back inside the next step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--layout aos|soa] [--no-host-path]
 
-The same run also times cp_lookup_decode_host on the same table placed in
-pinned host DRAM ("host_path" in the JSON line, against the measured
-host-to-device copy bandwidth), unless --no-host-path.
+At N = 1 the same run also times cp_lookup_decode_host on the same table placed
+in pinned host DRAM ("host_path" in the JSON line, against the measured
+host-to-device copy bandwidth; unless --no-host-path), the fused readout, the
+mixed-rate table, the encoder, the other table configs and the CPU oracle.
+Under torchrun these single-GPU legs are skipped; the e2e figure is then the
+whole job's (all ranks' lookups over the slowest rank's time).
 
 Under torchrun (N > 1) every rank holds its own replica of the table and
 decodes its own replay (seed + rank); no collective touches the data path
@@ -386,12 +389,15 @@ def our_arm(args, w, rank, world, local):
     peak, peak_kind = measured_peaks()
 
     others = None
-    if rank == 0 and not args.no_other_configs:
+    # single-GPU characterisation legs run at N = 1 only (they would hold every
+    # GPU of a multi-rank job while rank 0 alone works)
+    solo = world == 1
+    if solo and not args.no_other_configs:
         others = other_configs(args, w, table, idx, out, flush, stream)
 
     # Decode fused with a weighted readout over each token's 24 rows of a layer.
     fused = None
-    if w.d in (256, 512, 1024) and w.rows_per_token % 24 == 0:
+    if solo and w.d in (256, 512, 1024) and w.rows_per_token % 24 == 0:
         group = 24
         gates = torch.rand(n, dtype=torch.float32, device="cuda",
                            generator=torch.Generator(device="cuda").manual_seed(5))
@@ -416,7 +422,7 @@ def our_arm(args, w, rank, world, local):
     # Mixed per-row bit rates (frequency-based allocation): 2^24 rows x the same d,
     # rates uniform over b = 1.5 .. 3, the same replay shape.
     mixed = None
-    if w.d % 32 == 0 and w.d <= 4096 and rank == 0:
+    if w.d % 32 == 0 and w.d <= 4096 and solo:
         mrows = 1 << 24
         ks = synth.mixed_rates(synth.SEED_TABLE, torch.arange(mrows, device="cuda"))
         moffs = synth.mixed_offsets(ks, w.d)
@@ -439,7 +445,7 @@ def our_arm(args, w, rank, world, local):
         del mbuf, moffs, ks, midx
 
     # Offline compression on the GPU (the step before the hot path).
-    enc = encoder_measure(args, w) if rank == 0 and w.d >= 16 else None
+    enc = encoder_measure(args, w) if solo and w.d >= 16 else None
 
     # End to end through the public API: ids from pinned host memory, rows back
     # to pinned host memory, both copies inside the timed region.
@@ -452,10 +458,10 @@ def our_arm(args, w, rank, world, local):
         cp.lookup_decode(table, idx_d, out_h, stream)
 
     te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream)
-    e2e_value = n / float(te.mean())
+    _, e2e_value = aggregate(float(te.sum()), n * args.e2e_steps, world, dist, "cuda")
 
     host_obj = None
-    if not args.no_host_path and rank == 0 and w.residency in ("device", "host") \
+    if not args.no_host_path and solo and w.residency in ("device", "host") \
             and w.d >= 256:
         del rec, soa
         table.close()
@@ -463,7 +469,7 @@ def our_arm(args, w, rank, world, local):
         host_obj = host_path_measure(args, w, idx, flush, stream)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if solo and not args.no_cpu_baseline:
         rate, m, nt = oracle_sample_rate(w, idx_np, args.cpu_seconds, cp.default_lut())
         rate1, m1, _ = oracle_sample_rate(w, idx_np, args.cpu_seconds / 4, cp.default_lut(), 1)
         cpu = {"value": rate, "unit": "rows/s", "cores": nt, "kind": "oracle",

@@ -98,8 +98,8 @@ uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot) {
 cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                         cudaStream_t stream, bool host_path, const HostScratch* hs) {
   const bool soa = (t->layout == CP_LAYOUT_SOA);
-  const int pf = host_path ? cpk::kPfHost : cpk::kPfDevice;
   const int ci = cpk::cpl_index(t->d);
+  const int pf = host_path ? cpk::kPfHost : cpk::device_pf(ci);
   cpk::DecodeFn fn = host_path ? t->kernels.host[soa ? 1 : 0][ci] : t->kernels.dev[soa ? 1 : 0][ci];
   cpk::DecodeParams p;
   std::memset(&p, 0, sizeof(p));

@@ -5,11 +5,12 @@
 namespace cpk {
 
 namespace {
-template <bool SOA, int PF, bool PERM, int REP>
+// row[i]: chunks-per-lane index i; PF_SHORT stages for i = 1, 2, PF for the rest
+template <bool SOA, int PF, bool PERM, int REP, int PF_SHORT = PF>
 void fill(DecodeFn* row) {
   row[0] = &lookup_decode_kernel<6, SOA, PF, 0, PERM, REP>;
-  row[1] = &lookup_decode_kernel<6, SOA, PF, 1, PERM, REP>;
-  row[2] = &lookup_decode_kernel<6, SOA, PF, 2, PERM, REP>;
+  row[1] = &lookup_decode_kernel<6, SOA, PF_SHORT, 1, PERM, REP>;
+  row[2] = &lookup_decode_kernel<6, SOA, PF_SHORT, 2, PERM, REP>;
   row[3] = &lookup_decode_kernel<6, SOA, PF, 4, PERM, REP>;
   row[4] = &lookup_decode_kernel<6, SOA, PF, 8, PERM, REP>;
   row[5] = &lookup_decode_kernel<6, SOA, PF, 16, PERM, REP>;
@@ -18,8 +19,8 @@ void fill(DecodeFn* row) {
 
 KernelSet kernels_k6() {
   KernelSet s;
-  fill<false, kPfDevice, false, kLutRepDevice>(s.dev[0]);
-  fill<true, kPfDevice, false, kLutRepDevice>(s.dev[1]);
+  fill<false, kPfDevice, false, kLutRepDevice, kPfDeviceShort>(s.dev[0]);
+  fill<true, kPfDevice, false, kLutRepDevice, kPfDeviceShort>(s.dev[1]);
   fill<false, kPfHost, true, kLutRepHost>(s.host[0]);
   fill<true, kPfHost, true, kLutRepHost>(s.host[1]);
   s.host[0][1] = &lookup_decode_host_kernel<6, false, kPfHostReg, 1, 32>;

@@ -228,7 +228,7 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
   const int pf = cpk::kPfDevice;
   int nwarps = cpk::kMaxWarps;
   auto smem_for = [&](int w) {
-    return static_cast<size_t>(cpk::lut_bytes(32)) +
+    return static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepDevice)) +
            static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
   };
   while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;

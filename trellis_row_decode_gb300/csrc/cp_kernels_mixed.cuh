@@ -19,7 +19,7 @@ template <int CPL>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     lookup_decode_mixed_kernel(const DecodeParams p, const uint64_t* __restrict__ offsets) {
   constexpr int PF = kPfDevice;
-  constexpr int REP = 32;
+  constexpr int REP = kLutRepDevice;                   // as the single-rate kernel
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31;

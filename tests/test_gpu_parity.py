@@ -43,12 +43,12 @@ def _assert_exact(got, ref, what=""):
 # Full element-by-element parity at oracle-sized cases.
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("n", [4099, 10007])   # ragged against warps and batches of 32
 @pytest.mark.parametrize("layout", [cp.CP_LAYOUT_AOS, cp.CP_LAYOUT_SOA])
 @pytest.mark.parametrize("k", [3, 4, 5, 6])
 @pytest.mark.parametrize("d", [256, 512, 1024])
-def test_full_parity(lut, d, k, layout):
+def test_full_parity(lut, d, k, layout, n):
     n_rows = 3001                      # odd: the table's end is not 16-byte aligned
-    n = 10007                          # ragged against warps and batches of 32
     rec = device_table(SEED, n_rows, d, k)
     soa = None
     if layout == cp.CP_LAYOUT_SOA:

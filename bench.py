@@ -338,6 +338,19 @@ def time_steps(fn, steps, warmup, flush, stream):
     return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
 
 
+def hbm_same_run(flush, stream, steps: int = 20):
+    """Context for the HBM roofline, taken on this GPU in this run with a library
+    kernel: a 1 GiB device-to-device copy, read + write bytes counted."""
+    import torch
+    src = torch.ones(1 << 30, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    tc = time_steps(lambda: dst.copy_(src), steps, 3, flush, stream)
+    del src, dst
+    return {"copy_gbs": 2 * (1 << 30) / float(np.median(tc)) / 1e9,
+            "copy": "torch copy_ of a 1 GiB device buffer, read + write bytes, median of "
+                    f"{steps}, L2 flushed between"}
+
+
 def aggregate(local_time_s: float, local_units: int, world: int, dist, device):
     """Max of the ranks' timed totals and the whole-job throughput.
 
@@ -392,6 +405,9 @@ def our_arm(args, w, rank, world, local):
     # single-GPU characterisation legs run at N = 1 only (they would hold every
     # GPU of a multi-rank job while rank 0 alone works)
     solo = world == 1
+    ctx = hbm_same_run(flush, stream) if solo else None
+    if ctx is not None:
+        ctx["decode_frac_of_copy"] = achieved / ctx["copy_gbs"]
     if solo and not args.no_other_configs:
         others = other_configs(args, w, table, idx, out, flush, stream)
 
@@ -498,7 +514,7 @@ def our_arm(args, w, rank, world, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": ncu_traffic(w.name, args.layout),
-                         "bytes_per_lookup": bpl, "kernel": "lookup_decode_kernel"},
+                         "bytes_per_lookup": bpl, "kernel": "lookup_decode_block_kernel"},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": n * 8,
                     "path": "ids copied from pinned host memory; rows written by the decode kernel into pinned host memory",
                     "d2h_bytes_per_step": n * w.d * 2},
@@ -509,6 +525,8 @@ def our_arm(args, w, rank, world, local):
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
+        if ctx is not None:
+            line["hbm_same_run"] = ctx
         if host_obj is not None:
             line["host_path"] = host_obj
         if fused is not None:

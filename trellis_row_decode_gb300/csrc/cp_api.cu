@@ -99,7 +99,6 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
                         cudaStream_t stream, bool host_path, const HostScratch* hs) {
   const bool soa = (t->layout == CP_LAYOUT_SOA);
   const int ci = cpk::cpl_index(t->d);
-  const int pf = host_path ? cpk::kPfHost : cpk::device_pf(ci);
   cpk::DecodeFn fn = host_path ? t->kernels.host[soa ? 1 : 0][ci] : t->kernels.dev[soa ? 1 : 0][ci];
   cpk::DecodeParams p;
   std::memset(&p, 0, sizeof(p));
@@ -117,10 +116,35 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   p.out = out;
   p.status = t->status_dev;
 
-  const bool reg_ring = host_path && cpk::host_uses_register_ring(ci);
+  if (!host_path) {
+    // Non-persistent grid: kBlkWarps * kBlkRows lookups per CTA.
+    const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepBlock)) +
+                        static_cast<size_t>(cpk::kBlkWarps) * cpk::kBlkRows * p.stage_bytes;
+    if (smem > static_cast<size_t>(t->max_smem)) {
+      g_last_error = "geometry needs more shared memory than the device offers";
+      return CP_ERR_INVALID_ARG;
+    }
+    const uint64_t per_block = static_cast<uint64_t>(cpk::kBlkWarps) * cpk::kBlkRows;
+    const uint64_t blocks = (n + per_block - 1) / per_block;
+    if (blocks > 0x7FFFFFFFull) {
+      g_last_error = "too many lookups for one launch";
+      return CP_ERR_INVALID_ARG;
+    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    void* args[] = {&p};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
+                         dim3(cpk::kBlkWarps * 32), args, smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
+    return CP_OK;
+  }
+  // Host-resident table: persistent grid.
+  const int pf = cpk::kPfHost;
+  const bool reg_ring = cpk::host_uses_register_ring(ci);
   int nwarps = reg_ring ? cpk::kHostWarps : cpk::kMaxWarps;
-  const size_t lut = cpk::lut_bytes(reg_ring ? 32 : (host_path ? cpk::kLutRepHost
-                                                               : cpk::kLutRepDevice));
+  const size_t lut = cpk::lut_bytes(reg_ring ? 32 : cpk::kLutRepHost);
   auto smem_for = [&](int w) {
     if (reg_ring) return lut + static_cast<size_t>(w) * p.stage_bytes;   // one stage per warp
     return lut + static_cast<size_t>(w) * pf * p.stage_bytes + static_cast<size_t>(w) * pf * 8;
@@ -143,17 +167,10 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     g_last_error = "too many lookups for one launch";
     return CP_ERR_INVALID_ARG;
   }
-  if (!host_path) {
-    void* args[] = {&p};
-    e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
-                         dim3(nwarps * 32), args, smem, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "lookup-decode launch");
-    return CP_OK;
-  }
-  // Host-resident table, per pass of at most hs->capacity lookups: elect one
-  // owner per distinct id, partition the owners by row range, decode them in
-  // that order (each row lands at its own position), then fill the other
-  // lookups from their owner's row.
+  // Per pass of at most hs->capacity lookups: elect one owner per distinct id,
+  // partition the owners by row range, decode them in that order (each row
+  // lands at its own position), then fill the other lookups from their owner's
+  // row.
   unsigned long long* keys = hs->keys;
   uint32_t* owner = hs->owner;
   uint32_t* dup = hs->dup;
@@ -208,7 +225,7 @@ using cpx::kMaxLookups;
 using cpx::kMaxRows;
 using cpx::soa_stride;
 
-// Mixed-rate table: the HBM-path kernel with the rate chosen per row.
+// Mixed-rate table: a persistent decode kernel with the rate chosen per row.
 cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                        cudaStream_t stream) {
   cpk::DecodeParams p;
@@ -225,10 +242,10 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
   p.n = n;
   p.out = out;
   p.status = t->status_dev;
-  const int pf = cpk::kPfDevice;
+  const int pf = cpk::kPfMixed;
   int nwarps = cpk::kMaxWarps;
   auto smem_for = [&](int w) {
-    return static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepDevice)) +
+    return static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepMixed)) +
            static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
   };
   while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;

@@ -5,22 +5,32 @@
 namespace cpk {
 
 namespace {
-// row[i]: chunks-per-lane index i; PF_SHORT stages for i = 1, 2, PF for the rest
-template <bool SOA, int PF, bool PERM, int REP, int PF_SHORT = PF>
+// row[i]: chunks-per-lane index i
+template <bool SOA, int PF, bool PERM, int REP>
 void fill(DecodeFn* row) {
   row[0] = &lookup_decode_kernel<3, SOA, PF, 0, PERM, REP>;
-  row[1] = &lookup_decode_kernel<3, SOA, PF_SHORT, 1, PERM, REP>;
-  row[2] = &lookup_decode_kernel<3, SOA, PF_SHORT, 2, PERM, REP>;
+  row[1] = &lookup_decode_kernel<3, SOA, PF, 1, PERM, REP>;
+  row[2] = &lookup_decode_kernel<3, SOA, PF, 2, PERM, REP>;
   row[3] = &lookup_decode_kernel<3, SOA, PF, 4, PERM, REP>;
   row[4] = &lookup_decode_kernel<3, SOA, PF, 8, PERM, REP>;
   row[5] = &lookup_decode_kernel<3, SOA, PF, 16, PERM, REP>;
+}
+
+template <bool SOA>
+void fill_block(DecodeFn* row) {
+  row[0] = &lookup_decode_block_kernel<3, SOA, 0, kLutRepBlock, kBlkRows>;
+  row[1] = &lookup_decode_block_kernel<3, SOA, 1, kLutRepBlock, kBlkRows>;
+  row[2] = &lookup_decode_block_kernel<3, SOA, 2, kLutRepBlock, kBlkRows>;
+  row[3] = &lookup_decode_block_kernel<3, SOA, 4, kLutRepBlock, kBlkRows>;
+  row[4] = &lookup_decode_block_kernel<3, SOA, 8, kLutRepBlock, kBlkRows>;
+  row[5] = &lookup_decode_block_kernel<3, SOA, 16, kLutRepBlock, kBlkRows>;
 }
 }  // namespace
 
 KernelSet kernels_k3() {
   KernelSet s;
-  fill<false, kPfDevice, false, kLutRepDevice, kPfDeviceShort>(s.dev[0]);
-  fill<true, kPfDevice, false, kLutRepDevice, kPfDeviceShort>(s.dev[1]);
+  fill_block<false>(s.dev[0]);
+  fill_block<true>(s.dev[1]);
   fill<false, kPfHost, true, kLutRepHost>(s.host[0]);
   fill<true, kPfHost, true, kLutRepHost>(s.host[1]);
   s.host[0][1] = &lookup_decode_host_kernel<3, false, kPfHostReg, 1, 32>;

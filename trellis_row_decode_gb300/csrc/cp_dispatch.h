@@ -4,6 +4,7 @@
 #include "cp_kernels.cuh"
 #include "cp_kernels_host.cuh"
 #include "cp_kernels_reduce.cuh"
+#include "cp_kernels_mixed.cuh"
 
 namespace cpk {
 
@@ -33,14 +34,6 @@ void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, ui
 constexpr int kCplVariants = 6;
 constexpr int kCplValues[kCplVariants] = {0, 1, 2, 4, 8, 16};
 
-// Record-ring stages of the HBM path per chunks-per-lane index: d = 256 and 512
-// keep three rows in flight per warp (2-4 % faster at d = 512); d >= 1024 and
-// the any-d kernel keep one (its long rows would not fit 32 warps' stages).
-constexpr int kPfDeviceShort = 4;
-constexpr int device_pf(int cpl_idx) {
-  return (cpl_idx == 1 || cpl_idx == 2) ? kPfDeviceShort : kPfDevice;
-}
-
 inline int cpl_index(uint32_t d) {
   for (int i = 1; i < kCplVariants; ++i)
     if (d == 256u * static_cast<uint32_t>(kCplValues[i])) return i;
@@ -48,7 +41,8 @@ inline int cpl_index(uint32_t d) {
 }
 
 struct KernelSet {
-  DecodeFn dev[2][kCplVariants];    // [layout AoS/SoA][cpl index], lookup order
+  DecodeFn dev[2][kCplVariants];    // [layout AoS/SoA][cpl index]: non-persistent block
+                                    // kernel, lookup order
   DecodeFn host[2][kCplVariants];   // bucketed order: register-ring kernel for cpl
                                     // indices 1..3 (d <= 1024), cp.async kernel otherwise
   ReduceFn reduce[2][3];            // decode + group readout, d = 256, 512, 1024

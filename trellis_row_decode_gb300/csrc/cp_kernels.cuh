@@ -7,19 +7,29 @@
 // writes the rows in the original lookup order, duplicates included.
 //
 // Work mapping (GB300: 152 SMs, 228 KB shared memory per SM):
-//   * one persistent CTA of up to 32 warps per SM; each warp owns a contiguous
-//     range of lookups and decodes one row at a time;
+//   * HBM-resident tables: a non-persistent grid of small CTAs (8 warps, 4 rows
+//     per warp, 32 consecutive lookups per CTA).  The hardware block scheduler
+//     hands CTAs to SMs as they free up, so the 2 KB row writes advance through
+//     the output in a narrow window and SMs that reach memory faster (the
+//     imbalance between SMs is systematic on this part) take more CTAs.  With
+//     ~40 rows per warp in static ranges, a persistent grid ran 10-20 % longer;
+//   * host-resident tables (bucketed order): one persistent CTA per SM, each
+//     warp a contiguous range of positions and a ring of PF record stages, PF-1
+//     rows ahead of the row being decoded;
 //   * the record of a row is copied with 16-byte cp.async (L2 only) into a
-//     per-warp ring of PF shared-memory stages, PF-1 rows ahead of the row being
-//     decoded, so record latency overlaps decode and stores; the last 16-byte
-//     piece of the table is clamped with the copy's source size (zero fill);
+//     shared-memory stage; the block kernel queues all of a warp's rows before
+//     the CTA builds its LUT, so record latency overlaps the fill; the last
+//     16-byte piece of the table is clamped with the copy's source size (zero
+//     fill);
 //   * the shared LUT (512 fp16 pairs) is expanded in shared memory to 1024
-//     entries (the sign of y1 folded in, indexed by hash bits 14..23) and
-//     replicated 32 times, word (entry * 32 + lane): every lane reads its own
-//     bank, so a warp-wide LUT read is one wavefront.  The host-resident
-//     variant is bound by the host link, whose throughput here grows with the
-//     bytes in flight; it keeps 4 replicas (16 KB) and spends the shared memory
-//     on a deeper record ring instead;
+//     entries (the sign of y1 folded in, indexed by hash bits 14..23) with REP
+//     copies of each entry, word (entry * REP + lane % REP).  REP = 32 makes a
+//     warp-wide LUT read one wavefront; fewer copies cost bank conflicts (about
+//     3 wavefronts at REP = 2) but a smaller fill: the block kernel, which fills
+//     once per 32 rows, keeps 2 copies (8 KB); the persistent kernels keep 16
+//     (device, filled once per SM) or 4 (host: the shared memory goes to a
+//     deeper record ring, since the host link's throughput grows with the bytes
+//     in flight);
 //   * a record lands 16 bytes into its stage; once it has arrived, lane 0 copies
 //     the code's last 16 bits (a whole halfword, since d*k/16 is even) to the
 //     two bytes just below code bit 0, so the tail-biting wrap (windows that
@@ -179,25 +189,142 @@ __device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uin
   }
 }
 
-// Launch constants of the HBM-resident path: stages per warp (one row ahead)
-// and LUT replicas.  16 replicas: a warp's LUT read takes about 1.5 shared
-// wavefronts (lanes l and l + 16 share a replica) instead of 1, which the
-// memory-bound decode does not notice, and the per-launch fill is half of 32
-// replicas' (64 KB per CTA instead of 128 KB).
-#ifndef CP_PF_DEVICE
-#define CP_PF_DEVICE 2
+// Non-persistent kernel of the HBM-resident path: a CTA of kBlkWarps warps
+// decodes kBlkRows rows per warp, with its own LUT of kLutRepBlock replicas.
+#ifndef CP_BLK_WARPS
+#define CP_BLK_WARPS 8
 #endif
-constexpr int kPfDevice = CP_PF_DEVICE;
-constexpr int kLutRepDevice = 16;
+#ifndef CP_BLK_ROWS
+#define CP_BLK_ROWS 4
+#endif
+#ifndef CP_BLK_REP
+#define CP_BLK_REP 2
+#endif
+constexpr int kBlkWarps = CP_BLK_WARPS;
+constexpr int kBlkRows = CP_BLK_ROWS;
+constexpr int kLutRepBlock = CP_BLK_REP;
 
 // Byte offset of the record data inside a stage (room for the spliced tail).
 constexpr uint32_t kStagePrefix = 16;
 
+// Expand the 512 LUT pairs into shared memory: entry e -> pair e & 511 with y1
+// negated for e >= 512, REP copies of each entry (word e * REP + replica).
+template <int REP>
+__device__ __forceinline__ void fill_lut(uint8_t* smem, const uint32_t* lut, int tid, int nthreads) {
+  static_assert(REP >= 1 && REP <= 32 && (REP & (REP - 1)) == 0, "REP: power of two");
+  auto entry = [&](int e) {
+    const uint32_t v = __ldg(lut + (e & 511));
+    return (e & 512) ? (v ^ 0x80000000u) : v;
+  };
+  for (int q = tid; q < kLutEntries * REP / 4; q += nthreads) {   // one uint4 = 4 words
+    uint4 u;
+    if constexpr (REP >= 4) {
+      const uint32_t v = entry(q / (REP / 4));
+      u = make_uint4(v, v, v, v);
+    } else {
+      u = make_uint4(entry(4 * q / REP), entry((4 * q + 1) / REP), entry((4 * q + 2) / REP),
+                     entry((4 * q + 3) / REP));
+    }
+    reinterpret_cast<uint4*>(smem)[q] = u;
+  }
+}
+
+// Queue (one warp, warp-uniform r) the 16-byte cp.async copies of record r into
+// the stage whose data starts at shared address sa.  Returns the stage's meta
+// word: bit 0 = record present, bit 1 = r odd (SoA alpha half), bits 8.. = the
+// record's misalignment; 0 when r is outside [0, n_rows) (lane 0 then sets the
+// status bit).  The caller commits the group.
+template <bool SOA, bool ONE_PASS>
+__device__ __forceinline__ uint32_t issue_record(const DecodeParams& p, int64_t r, uint32_t sa,
+                                                 uint32_t lane) {
+  if (static_cast<uint64_t>(r) >= p.n_rows) {           // also rejects r < 0
+    if (lane == 0) atomicOr(p.status, 1u);
+    return 0;
+  }
+  const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
+  const uintptr_t tbl_end = codes + p.table_bytes;
+  const uintptr_t a = codes + static_cast<uint64_t>(r) * p.stride;
+  const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
+  const uint32_t mis = static_cast<uint32_t>(a - a0);
+  const uint32_t nch = (mis + p.code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
+  auto copy = [&](uint32_t c) {
+    const uintptr_t src = a0 + 16u * c;
+    uint32_t bytes = 16;
+    if (!SOA) {
+      const uintptr_t left = tbl_end - src;             // > 0: src lies inside the table
+      bytes = left < 16 ? static_cast<uint32_t>(left) : 16u;
+    }
+    cp_async16(sa + 16u * c, reinterpret_cast<const void*>(src), bytes);
+  };
+  if constexpr (ONE_PASS) {
+    if (lane < nch) copy(lane);
+  } else {
+    for (uint32_t c = lane; c < nch; c += 32) copy(c);
+  }
+  if (SOA && lane == 31) {
+    const uint64_t r2 = static_cast<uint64_t>(r) & ~1ull;
+    // alpha_slot is measured from the stage start, like the decode's read
+    cp_async4(sa - kStagePrefix + p.alpha_slot, p.alpha + r2, (r2 + 1 < p.n_rows) ? 4u : 2u);
+  }
+  return 1u | ((static_cast<uint32_t>(r) & 1u) << 1) | (mis << 8);
+}
+
+// Decode the record that has landed in stage sb (data at sb + kStagePrefix) with
+// meta word m into orow, or write a row of zeros when m is 0.  Whole warp.
+template <int K, bool SOA, int CPL, int REP>
+__device__ __forceinline__ void decode_stage(const DecodeParams& p, uint8_t* sb, uint32_t m,
+                                             const uint8_t* lut, uint32_t lane, uint4* orow) {
+  const uint32_t code_bytes = p.code_bytes;
+  const uint32_t d = p.d;
+  if (m & 1u) {
+    const uint32_t mis = m >> 8;
+    uint8_t* code = sb + kStagePrefix + mis;
+    // Tail-biting splice: the code's last 16 bits just below bit 0.
+    if (lane == 0)
+      *reinterpret_cast<uint16_t*>(code - 2) =
+          *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+    const uint16_t abits = SOA ? *reinterpret_cast<const uint16_t*>(
+                                     sb + p.alpha_slot + 2 * ((m >> 1) & 1u))
+                               : *reinterpret_cast<const uint16_t*>(code + code_bytes);
+    __syncwarp();
+    const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
+    const uint32_t ex = (abits >> 7) & 0xFFu;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(sb);
+    const uint32_t boff = (kStagePrefix + mis) * 8;
+    if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {   // |alpha| in [2^-14, 2^16) or 0
+      const __half ah = __float2half_rn(a);               // exact in this range
+      decode_row<K, CPL, true, REP>(w, boff, d, lut, lane, __half_as_ushort(ah), a, orow);
+    } else {
+      decode_row<K, CPL, false, REP>(w, boff, d, lut, lane, 0, a, orow);
+    }
+  } else {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
+  }
+}
+
+// cp.async.wait_group with a count known only after unrolling (0..7; larger
+// counts wait for every group, which is also correct).
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  switch (n) {
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    default: cp_async_wait<0>(); break;
+  }
+}
+
+// Persistent kernel: one CTA of up to kMaxWarps warps per SM, each warp a
+// contiguous range of positions, a ring of PF record stages per warp.
 // K: bits per step (3..6).  SOA: read the SoA copy.  PF: stages per warp.
 // CPL: chunks per lane when d == 256 * CPL, 0 for any d (runtime loop).
 // PERM: lookups are visited in the order p.perm (rows still land at their own
 // output position); used to give host-resident tables address locality.
-// REP: LUT replicas in shared memory (16 or 4).
+// REP: LUT replicas in shared memory.
 template <int K, bool SOA, int PF, int CPL, bool PERM, int REP>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -206,29 +333,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
 
-  // Shared LUT: entry e -> pair e & 511, y1 negated for e >= 512; REP copies.
   constexpr int kLutBytes = lut_bytes(REP);
-  for (int q = tid; q < kLutEntries * REP / 4; q += blockDim.x) {
-    const int e = q / (REP / 4);                        // REP / 4 uint4 per entry
-    uint32_t v = __ldg(p.lut + (e & 511));
-    if (e & 512) v ^= 0x80000000u;
-    reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
-  }
+  fill_lut<REP>(smem, p.lut, tid, blockDim.x);
   __syncthreads();
 
-  // Parameters held in registers for the whole loop.
   const uint32_t stage_bytes = p.stage_bytes;
-  const uint32_t code_bytes = p.code_bytes;
   const uint32_t d = p.d;
-  const uint64_t n_rows = p.n_rows;
-  const uint64_t stride = p.stride;
-  const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
-  const uintptr_t tbl_end = codes + p.table_bytes;
   // Records up to 496 bytes (d <= 1024 here) fit one 16-byte copy per lane.
   constexpr bool kOnePass = (CPL >= 1 && CPL <= 4);
 
   uint8_t* stages = smem + kLutBytes + static_cast<size_t>(warp) * PF * stage_bytes;
-  // per stage: [0] flags | misalignment << 8, [1] output row (PERM)
+  // per stage: [0] meta word, [1] output row (PERM)
   uint32_t* meta = reinterpret_cast<uint32_t*>(smem + kLutBytes +
                                                static_cast<size_t>(nwarps) * PF * stage_bytes) +
                    warp * PF * 2;
@@ -279,36 +394,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
     uint32_t jrow = 0;
     if (PERM) jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
     const uint32_t st = q & (PF - 1);
-    const uint32_t sa = stages_sa + st * stage_bytes;
-    uint32_t m = 0;
-    if (static_cast<uint64_t>(r) < n_rows) {            // also rejects r < 0
-      const uintptr_t a = codes + static_cast<uint64_t>(r) * stride;
-      const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
-      const uint32_t mis = static_cast<uint32_t>(a - a0);
-      const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;
-      auto copy = [&](uint32_t c) {
-        const uintptr_t src = a0 + 16u * c;
-        uint32_t bytes = 16;
-        if (!SOA) {
-          const uintptr_t left = tbl_end - src;           // > 0: src lies inside the table
-          bytes = left < 16 ? static_cast<uint32_t>(left) : 16u;
-        }
-        cp_async16(sa + 16u * c, reinterpret_cast<const void*>(src), bytes);
-      };
-      if constexpr (kOnePass) {
-        if (lane < nch) copy(lane);
-      } else {
-        for (uint32_t c = lane; c < nch; c += 32) copy(c);
-      }
-      if (SOA && lane == 31) {
-        const uint64_t r2 = static_cast<uint64_t>(r) & ~1ull;
-        // alpha_slot is measured from the stage start, like the decode's read
-        cp_async4(sa - kStagePrefix + p.alpha_slot, p.alpha + r2, (r2 + 1 < n_rows) ? 4u : 2u);
-      }
-      m = 1u | ((static_cast<uint32_t>(r) & 1u) << 1) | (mis << 8);
-    } else if (lane == 0) {
-      atomicOr(p.status, 1u);
-    }
+    const uint32_t m = issue_record<SOA, kOnePass>(p, r, stages_sa + st * stage_bytes, lane);
     if (lane == 0) {
       meta[2 * st] = m;
       if (PERM) meta[2 * st + 1] = jrow;
@@ -322,7 +408,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
     else cp_async_commit();
   }
 
-  const uint4 zero = make_uint4(0, 0, 0, 0);
   uint4* orow_seq = reinterpret_cast<uint4*>(p.out) + lo * (d >> 3);
   for (uint32_t i = 0; i < cnt; ++i, orow_seq += (d >> 3)) {
     if (i + PF - 1 < cnt) issue(i + PF - 1);
@@ -331,36 +416,63 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
     __syncwarp();
 
     const uint32_t st = i & (PF - 1);
-    uint8_t* sb = stages + st * stage_bytes + kStagePrefix;
-    const uint32_t m = meta[2 * st];
     uint4* orow = PERM ? reinterpret_cast<uint4*>(p.out) +
                              static_cast<uint64_t>(meta[2 * st + 1]) * (d >> 3)
                        : orow_seq;
-    if (m & 1u) {
-      const uint32_t mis = m >> 8;
-      uint8_t* code = sb + mis;
-      // Tail-biting splice: the code's last 16 bits just below bit 0.
-      if (lane == 0)
-        *reinterpret_cast<uint16_t*>(code - 2) =
-            *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
-      const uint16_t abits = SOA ? *reinterpret_cast<const uint16_t*>(
-                                       sb - kStagePrefix + p.alpha_slot + 2 * ((m >> 1) & 1u))
-                                 : *reinterpret_cast<const uint16_t*>(code + code_bytes);
-      __syncwarp();
-      const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
-      const uint32_t ex = (abits >> 7) & 0xFFu;
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(sb - kStagePrefix);
-      const uint32_t boff = (kStagePrefix + mis) * 8;
-      if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {   // |alpha| in [2^-14, 2^16) or 0
-        const __half ah = __float2half_rn(a);             // exact in this range
-        decode_row<K, CPL, true, REP>(w, boff, d, smem, lane, __half_as_ushort(ah), a, orow);
-      } else {
-        decode_row<K, CPL, false, REP>(w, boff, d, smem, lane, 0, a, orow);
-      }
-    } else {
-      for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
-    }
+    decode_stage<K, SOA, CPL, REP>(p, stages + st * stage_bytes, meta[2 * st], smem, lane, orow);
     __syncwarp();
+  }
+}
+
+// Non-persistent kernel of the HBM-resident path.  CTA b decodes the lookups
+// [b * kBlkWarps * ROWS, (b + 1) * kBlkWarps * ROWS): warp w takes positions
+// w, w + kBlkWarps, ..., so at every step the CTA writes kBlkWarps consecutive
+// rows.  Each warp queues all of its ROWS record copies (one stage each) before
+// the CTA expands its LUT, so the record latency overlaps the fill.  The
+// hardware block scheduler hands CTAs to SMs as SMs free up, which keeps the
+// output writes in a narrow, advancing window of addresses and lets faster SMs
+// take more of the work; a persistent grid with static ranges per warp ran
+// 10-20 % longer on the same replay.
+template <int K, bool SOA, int CPL, int REP, int ROWS>
+__global__ void __launch_bounds__(kBlkWarps * 32) lookup_decode_block_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const uint32_t lane = tid & 31;
+  const int warp = tid >> 5;
+  constexpr bool kOnePass = (CPL >= 1 && CPL <= 4);
+  constexpr int kLutBytes = lut_bytes(REP);
+  const uint32_t stage_bytes = p.stage_bytes;
+  uint8_t* stages = smem + kLutBytes + static_cast<size_t>(warp) * ROWS * stage_bytes;
+  const uint32_t stages_sa = smem_addr(stages) + kStagePrefix;
+
+  const uint64_t first = static_cast<uint64_t>(blockIdx.x) * (kBlkWarps * ROWS) + warp;
+  const uint64_t n = p.n;
+  int64_t my_id = 0;                                  // lane t: id of the warp's row t
+  if (lane < static_cast<uint32_t>(ROWS)) {
+    const uint64_t j = first + static_cast<uint64_t>(lane) * kBlkWarps;
+    if (j < n) my_id = __ldg(p.idx + j);
+  }
+  uint32_t m[ROWS];
+#pragma unroll
+  for (int t = 0; t < ROWS; ++t) {
+    const int64_t r = __shfl_sync(0xffffffffu, my_id, t);
+    m[t] = 0;
+    if (first + static_cast<uint64_t>(t) * kBlkWarps < n)
+      m[t] = issue_record<SOA, kOnePass>(p, r, stages_sa + t * stage_bytes, lane);
+    cp_async_commit();
+  }
+
+  fill_lut<REP>(smem, p.lut, tid, kBlkWarps * 32);
+  __syncthreads();
+
+#pragma unroll
+  for (int t = 0; t < ROWS; ++t) {
+    const uint64_t j = first + static_cast<uint64_t>(t) * kBlkWarps;
+    if (j >= n) break;                                // later rows are past the end too
+    cp_async_wait_n(ROWS - 1 - t);
+    __syncwarp();
+    decode_stage<K, SOA, CPL, REP>(p, stages + t * stage_bytes, m[t], smem, lane,
+                                   reinterpret_cast<uint4*>(p.out) + j * (p.d >> 3));
   }
 }
 

@@ -6,7 +6,7 @@
 // 전제와 한계).  A mixed-rate table stores row r's record (code at rate k_r, then
 // the bf16 scale) at bytes [offsets[r], offsets[r+1]); k_r = (R_r - 2) * 16 / d
 // follows from the record length, so the offset table is the only extra data.
-// The kernel is the HBM-path kernel with the rate dispatched per row: each lane
+// The decode steps are the HBM-path kernel's, with the rate dispatched per row: each lane
 // loads its batch row's two offsets together with the id, and the decode picks
 // decode_row<k> by a warp-uniform switch.
 #pragma once
@@ -15,23 +15,25 @@
 
 namespace cpk {
 
+// Persistent grid, one CTA of kMaxWarps warps per SM: each row needs three
+// dependent loads (id, then its two offsets, then the record), which the batch
+// look-ahead of a persistent warp hides; the non-persistent form of the
+// single-rate kernel, which starts that chain once per CTA, ran 30 % slower here.
+constexpr int kPfMixed = 2;                            // record stages per warp
+constexpr int kLutRepMixed = 16;                       // LUT replicas (filled once per SM)
+
 template <int CPL>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     lookup_decode_mixed_kernel(const DecodeParams p, const uint64_t* __restrict__ offsets) {
-  constexpr int PF = kPfDevice;
-  constexpr int REP = kLutRepDevice;                   // as the single-rate kernel
+  constexpr int PF = kPfMixed;
+  constexpr int REP = kLutRepMixed;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31;
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   constexpr int kLutBytes = lut_bytes(REP);
-  for (int q = tid; q < kLutEntries * REP / 4; q += blockDim.x) {
-    const int e = q / (REP / 4);
-    uint32_t v = __ldg(p.lut + (e & 511));
-    if (e & 512) v ^= 0x80000000u;
-    reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
-  }
+  fill_lut<REP>(smem, p.lut, tid, blockDim.x);
   __syncthreads();
 
   const uint32_t stage_bytes = p.stage_bytes;

@@ -62,12 +62,16 @@ def test_full_parity(lut, d, k, layout, n):
     _assert_exact(got.reshape(n, d), ref, f"d={d} k={k} layout={layout}")
 
 
+@pytest.mark.parametrize("layout", [cp.CP_LAYOUT_AOS, cp.CP_LAYOUT_SOA])
 @pytest.mark.parametrize("d,k", [(8, 4), (16, 6), (32, 3), (32, 5), (64, 4), (2048, 5),
                                  (4096, 6), (4096, 3)])
-def test_parity_small_and_large_rows(lut, d, k):
+def test_parity_small_and_large_rows(lut, d, k, layout):
     n_rows, n = 777, 2049
     rec = device_table(SEED + 1, n_rows, d, k)
-    table = cp.load_table(rec, n_rows, d, k, lut)
+    soa = None
+    if layout == cp.CP_LAYOUT_SOA:
+        soa = torch.empty(cp.soa_bytes(n_rows, d, k), dtype=torch.uint8, device="cuda")
+    table = cp.load_table(rec, n_rows, d, k, lut, layout=layout, soa=soa)
     idx = synth.uniform_indices(7, n, n_rows)
     got = _run(table, idx)
     _assert_exact(got.reshape(n, d), oracle_decode(SEED + 1, d, k, idx, n_rows, lut), f"d={d}")

@@ -161,25 +161,39 @@ __device__ __forceinline__ uint64_t funnel64(uint32_t lo, uint32_t hi, uint32_t 
   return ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
 }
 
-// Decode one staged row into orow (16-byte chunks).  w: staged words; boff: bit
-// offset of code bit 0 in the stage (>= 16 bits of spliced tail below it).
-// CPL > 0: d == 256 * CPL.
+// Decode one staged row with LPR lanes (sub = this lane's index among them),
+// each lane CPL 16-byte chunks c = sub + LPR m, written to orow.  The chunks'
+// bit offsets boff + K(4c + 1) - 16 differ by K * LPR / 8 whole words, so one
+// shift amount serves all of them.  lane picks the LUT replica.
+template <int K, int CPL, bool F16, int REP, int LPR>
+__device__ __forceinline__ void decode_row_lanes(const uint32_t* w, uint32_t boff,
+                                                 const uint8_t* lut_bytes, uint32_t lane,
+                                                 uint32_t sub, uint16_t a_h, float a,
+                                                 uint4* orow) {
+  static_assert((K * LPR) % 8 == 0, "chunk offsets must be whole words");
+  const uint32_t lane4 = (lane & (REP - 1)) << 2;
+  const uint32_t P0 = boff + K * (4 * sub + 1) - 16;
+  const uint32_t* w0 = w + (P0 >> 5);
+  const uint32_t sh = P0 & 31;
+#pragma unroll
+  for (int m = 0; m < CPL; ++m) {
+    constexpr int kStep = K * LPR / 8;                  // words between consecutive chunks
+    const uint64_t x = funnel64(w0[kStep * m], w0[kStep * m + 1], sh);
+    __stcs(orow + sub + LPR * m, decode_chunk<K, F16, REP>(x, lut_bytes, lane4, a_h, a));
+  }
+}
+
+// Decode one staged row into orow (16-byte chunks) with the whole warp.  w:
+// staged words; boff: bit offset of code bit 0 in the stage (>= 16 bits of
+// spliced tail below it).  CPL > 0: d == 256 * CPL.
 template <int K, int CPL, bool F16, int REP>
 __device__ __forceinline__ void decode_row(const uint32_t* w, uint32_t boff, uint32_t d,
                                            const uint8_t* lut_bytes, uint32_t lane,
                                            uint16_t a_h, float a, uint4* orow) {
-  const uint32_t lane4 = (lane & (REP - 1)) << 2;
   if constexpr (CPL > 0) {
-    // chunk c = lane + 32 m starts at bit boff + K(4 lane + 1) - 16 + 128 K m
-    const uint32_t P0 = boff + K * (4 * lane + 1) - 16;
-    const uint32_t* w0 = w + (P0 >> 5);
-    const uint32_t sh = P0 & 31;
-#pragma unroll
-    for (int m = 0; m < CPL; ++m) {
-      const uint64_t x = funnel64(w0[4 * K * m], w0[4 * K * m + 1], sh);
-      __stcs(orow + lane + 32 * m, decode_chunk<K, F16, REP>(x, lut_bytes, lane4, a_h, a));
-    }
+    decode_row_lanes<K, CPL, F16, REP, 32>(w, boff, lut_bytes, lane, lane, a_h, a, orow);
   } else {
+    const uint32_t lane4 = (lane & (REP - 1)) << 2;
     const uint32_t C = d >> 3;
     for (uint32_t c = lane; c < C; c += 32) {
       const uint32_t P = boff + K * (4 * c + 1) - 16;
@@ -229,16 +243,17 @@ __device__ __forceinline__ void fill_lut(uint8_t* smem, const uint32_t* lut, int
   }
 }
 
-// Queue (one warp, warp-uniform r) the 16-byte cp.async copies of record r into
-// the stage whose data starts at shared address sa.  Returns the stage's meta
-// word: bit 0 = record present, bit 1 = r odd (SoA alpha half), bits 8.. = the
-// record's misalignment; 0 when r is outside [0, n_rows) (lane 0 then sets the
-// status bit).  The caller commits the group.
-template <bool SOA, bool ONE_PASS>
+// Queue the 16-byte cp.async copies of record r into the stage whose data starts
+// at shared address sa, with LPR lanes (sub = this lane's index among them; r is
+// the same on those lanes).  Returns the stage's meta word: bit 0 = record
+// present, bit 1 = r odd (SoA alpha half), bits 8.. = the record's misalignment;
+// 0 when r is outside [0, n_rows) (lane sub 0 then sets the status bit).  The
+// caller commits the group.  ONE_PASS: the record spans at most LPR pieces.
+template <bool SOA, bool ONE_PASS, int LPR = 32>
 __device__ __forceinline__ uint32_t issue_record(const DecodeParams& p, int64_t r, uint32_t sa,
-                                                 uint32_t lane) {
+                                                 uint32_t sub) {
   if (static_cast<uint64_t>(r) >= p.n_rows) {           // also rejects r < 0
-    if (lane == 0) atomicOr(p.status, 1u);
+    if (sub == 0) atomicOr(p.status, 1u);
     return 0;
   }
   const uintptr_t codes = reinterpret_cast<uintptr_t>(p.codes);
@@ -257,11 +272,11 @@ __device__ __forceinline__ uint32_t issue_record(const DecodeParams& p, int64_t 
     cp_async16(sa + 16u * c, reinterpret_cast<const void*>(src), bytes);
   };
   if constexpr (ONE_PASS) {
-    if (lane < nch) copy(lane);
+    if (sub < nch) copy(sub);
   } else {
-    for (uint32_t c = lane; c < nch; c += 32) copy(c);
+    for (uint32_t c = sub; c < nch; c += LPR) copy(c);
   }
-  if (SOA && lane == 31) {
+  if (SOA && sub == LPR - 1) {
     const uint64_t r2 = static_cast<uint64_t>(r) & ~1ull;
     // alpha_slot is measured from the stage start, like the decode's read
     cp_async4(sa - kStagePrefix + p.alpha_slot, p.alpha + r2, (r2 + 1 < p.n_rows) ? 4u : 2u);
@@ -270,36 +285,54 @@ __device__ __forceinline__ uint32_t issue_record(const DecodeParams& p, int64_t 
 }
 
 // Decode the record that has landed in stage sb (data at sb + kStagePrefix) with
-// meta word m into orow, or write a row of zeros when m is 0.  Whole warp.
-template <int K, bool SOA, int CPL, int REP>
+// meta word m into orow, or write a row of zeros when m is 0, with LPR lanes
+// (sub = this lane's index among them; every lane of the warp must call it, the
+// LPR-lane groups each with their own row).  CPL: chunks per lane of the group
+// (LPR * CPL * 8 == d), 0 for any d with the whole warp.  valid = false: the
+// group has no row (no store).
+template <int K, bool SOA, int CPL, int REP, int LPR = 32>
 __device__ __forceinline__ void decode_stage(const DecodeParams& p, uint8_t* sb, uint32_t m,
-                                             const uint8_t* lut, uint32_t lane, uint4* orow) {
+                                             const uint8_t* lut, uint32_t lane, uint32_t sub,
+                                             uint4* orow, bool valid) {
+  static_assert(CPL > 0 || LPR == 32, "the any-d decode uses the whole warp");
   const uint32_t code_bytes = p.code_bytes;
   const uint32_t d = p.d;
-  if (m & 1u) {
-    const uint32_t mis = m >> 8;
-    uint8_t* code = sb + kStagePrefix + mis;
-    // Tail-biting splice: the code's last 16 bits just below bit 0.
-    if (lane == 0)
-      *reinterpret_cast<uint16_t*>(code - 2) =
-          *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+  const bool has = (m & 1u) != 0;
+  const uint32_t mis = m >> 8;
+  uint8_t* code = sb + kStagePrefix + mis;
+  // Tail-biting splice: the code's last 16 bits just below bit 0.
+  if (has && sub == 0)
+    *reinterpret_cast<uint16_t*>(code - 2) =
+        *reinterpret_cast<const uint16_t*>(code + code_bytes - 2);
+  __syncwarp();
+  if (has) {
     const uint16_t abits = SOA ? *reinterpret_cast<const uint16_t*>(
                                      sb + p.alpha_slot + 2 * ((m >> 1) & 1u))
                                : *reinterpret_cast<const uint16_t*>(code + code_bytes);
-    __syncwarp();
     const float a = __uint_as_float(static_cast<uint32_t>(abits) << 16);
     const uint32_t ex = (abits >> 7) & 0xFFu;
     const uint32_t* w = reinterpret_cast<const uint32_t*>(sb);
     const uint32_t boff = (kStagePrefix + mis) * 8;
-    if ((abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u) {   // |alpha| in [2^-14, 2^16) or 0
-      const __half ah = __float2half_rn(a);               // exact in this range
-      decode_row<K, CPL, true, REP>(w, boff, d, lut, lane, __half_as_ushort(ah), a, orow);
+    const bool f16 = (abits & 0x7FFFu) == 0 || (ex - 113u) <= 29u;  // |alpha| in [2^-14, 2^16) or 0
+    if constexpr (CPL > 0) {
+      if (f16) {
+        const __half ah = __float2half_rn(a);             // exact in this range
+        decode_row_lanes<K, CPL, true, REP, LPR>(w, boff, lut, lane, sub, __half_as_ushort(ah), a,
+                                                 orow);
+      } else {
+        decode_row_lanes<K, CPL, false, REP, LPR>(w, boff, lut, lane, sub, 0, a, orow);
+      }
     } else {
-      decode_row<K, CPL, false, REP>(w, boff, d, lut, lane, 0, a, orow);
+      if (f16) {
+        const __half ah = __float2half_rn(a);
+        decode_row<K, 0, true, REP>(w, boff, d, lut, lane, __half_as_ushort(ah), a, orow);
+      } else {
+        decode_row<K, 0, false, REP>(w, boff, d, lut, lane, 0, a, orow);
+      }
     }
-  } else {
+  } else if (valid) {
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (uint32_t c = lane; c < (d >> 3); c += 32) __stcs(orow + c, zero);
+    for (uint32_t c = sub; c < (d >> 3); c += LPR) __stcs(orow + c, zero);
   }
 }
 
@@ -419,7 +452,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
     uint4* orow = PERM ? reinterpret_cast<uint4*>(p.out) +
                              static_cast<uint64_t>(meta[2 * st + 1]) * (d >> 3)
                        : orow_seq;
-    decode_stage<K, SOA, CPL, REP>(p, stages + st * stage_bytes, meta[2 * st], smem, lane, orow);
+    decode_stage<K, SOA, CPL, REP>(p, stages + st * stage_bytes, meta[2 * st], smem, lane, lane, orow,
+                                   true);
     __syncwarp();
   }
 }
@@ -433,12 +467,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
 // output writes in a narrow, advancing window of addresses and lets faster SMs
 // take more of the work; a persistent grid with static ranges per warp ran
 // 10-20 % longer on the same replay.
+// Rows shorter than 1024 (d = 256, 512) are decoded G = 1024 / d at a time by
+// groups of 32 / G lanes, each lane 4 chunks as at d = 1024: the per-row work
+// that does not scale with d (id, record issue, splice, scale) is then shared
+// by G rows per warp instruction.
 template <int K, bool SOA, int CPL, int REP, int ROWS>
 __global__ void __launch_bounds__(kBlkWarps * 32) lookup_decode_block_kernel(const DecodeParams p) {
+  constexpr int G = (CPL == 1) ? 4 : (CPL == 2) ? 2 : 1;   // rows side by side in a warp
+  constexpr int LPR = 32 / G;                               // lanes per row
+  constexpr int CPLG = CPL * G;                             // chunks per lane
+  constexpr int STEPS = ROWS / G;
+  static_assert(ROWS % G == 0, "rows per warp must be a multiple of the rows per step");
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31;
   const int warp = tid >> 5;
+  const uint32_t slot = lane / LPR;                         // this lane's row within a step
+  const uint32_t sub = lane % LPR;
+  // Records up to 16 * LPR bytes fit one 16-byte copy per lane of the group:
+  // d * k / 16 + 2 + 14 <= d / 2 for k <= 6 and d >= 128.
   constexpr bool kOnePass = (CPL >= 1 && CPL <= 4);
   constexpr int kLutBytes = lut_bytes(REP);
   const uint32_t stage_bytes = p.stage_bytes;
@@ -452,13 +499,14 @@ __global__ void __launch_bounds__(kBlkWarps * 32) lookup_decode_block_kernel(con
     const uint64_t j = first + static_cast<uint64_t>(lane) * kBlkWarps;
     if (j < n) my_id = __ldg(p.idx + j);
   }
-  uint32_t m[ROWS];
+  uint32_t m[STEPS];
 #pragma unroll
-  for (int t = 0; t < ROWS; ++t) {
-    const int64_t r = __shfl_sync(0xffffffffu, my_id, t);
-    m[t] = 0;
+  for (int s = 0; s < STEPS; ++s) {
+    const uint32_t t = s * G + slot;                  // row of this lane's group
+    const int64_t r = __shfl_sync(0xffffffffu, my_id, static_cast<int>(t));
+    m[s] = 0;
     if (first + static_cast<uint64_t>(t) * kBlkWarps < n)
-      m[t] = issue_record<SOA, kOnePass>(p, r, stages_sa + t * stage_bytes, lane);
+      m[s] = issue_record<SOA, kOnePass, LPR>(p, r, stages_sa + t * stage_bytes, sub);
     cp_async_commit();
   }
 
@@ -466,13 +514,15 @@ __global__ void __launch_bounds__(kBlkWarps * 32) lookup_decode_block_kernel(con
   __syncthreads();
 
 #pragma unroll
-  for (int t = 0; t < ROWS; ++t) {
+  for (int s = 0; s < STEPS; ++s) {
+    const uint32_t t = s * G + slot;
     const uint64_t j = first + static_cast<uint64_t>(t) * kBlkWarps;
-    if (j >= n) break;                                // later rows are past the end too
-    cp_async_wait_n(ROWS - 1 - t);
+    if (first + static_cast<uint64_t>(s * G) * kBlkWarps >= n) break;   // no row of this step
+    cp_async_wait_n(STEPS - 1 - s);
     __syncwarp();
-    decode_stage<K, SOA, CPL, REP>(p, stages + t * stage_bytes, m[t], smem, lane,
-                                   reinterpret_cast<uint4*>(p.out) + j * (p.d >> 3));
+    decode_stage<K, SOA, CPLG, REP, LPR>(p, stages + t * stage_bytes, m[s], smem, lane, sub,
+                                         reinterpret_cast<uint4*>(p.out) + j * (p.d >> 3),
+                                         j < n);
   }
 }
 

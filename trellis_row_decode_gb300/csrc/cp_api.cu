@@ -117,14 +117,15 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   p.status = t->status_dev;
 
   if (!host_path) {
-    // Non-persistent grid: kBlkWarps * kBlkRows lookups per CTA.
+    // Non-persistent grid: kBlkWarps * block_rows(ci) lookups per CTA.
+    const int rows = cpk::block_rows(ci);
     const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepBlock)) +
-                        static_cast<size_t>(cpk::kBlkWarps) * cpk::kBlkRows * p.stage_bytes;
+                        static_cast<size_t>(cpk::kBlkWarps) * rows * p.stage_bytes;
     if (smem > static_cast<size_t>(t->max_smem)) {
       g_last_error = "geometry needs more shared memory than the device offers";
       return CP_ERR_INVALID_ARG;
     }
-    const uint64_t per_block = static_cast<uint64_t>(cpk::kBlkWarps) * cpk::kBlkRows;
+    const uint64_t per_block = static_cast<uint64_t>(cpk::kBlkWarps) * rows;
     const uint64_t blocks = (n + per_block - 1) / per_block;
     if (blocks > 0x7FFFFFFFull) {
       g_last_error = "too many lookups for one launch";

@@ -34,6 +34,16 @@ void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, ui
 constexpr int kCplVariants = 6;
 constexpr int kCplValues[kCplVariants] = {0, 1, 2, 4, 8, 16};
 
+// Rows per warp of the HBM block kernel per chunks-per-lane index: d = 256 and
+// 512 (two or four rows per warp step) may take more rows per CTA than the rest.
+#ifndef CP_BLK_ROWS_SHORT
+#define CP_BLK_ROWS_SHORT 4
+#endif
+constexpr int kBlkRowsShort = CP_BLK_ROWS_SHORT;
+constexpr int block_rows(int cpl_idx) {
+  return (cpl_idx == 1 || cpl_idx == 2) ? kBlkRowsShort : kBlkRows;
+}
+
 inline int cpl_index(uint32_t d) {
   for (int i = 1; i < kCplVariants; ++i)
     if (d == 256u * static_cast<uint32_t>(kCplValues[i])) return i;

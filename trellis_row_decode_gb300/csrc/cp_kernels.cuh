@@ -223,23 +223,35 @@ constexpr uint32_t kStagePrefix = 16;
 
 // Expand the 512 LUT pairs into shared memory: entry e -> pair e & 511 with y1
 // negated for e >= 512, REP copies of each entry (word e * REP + replica).
+// REP <= 4 (the block kernel fills once per 32 rows): one 8-byte load per two
+// source pairs, written with its sign-flipped twin 512 entries on.
 template <int REP>
 __device__ __forceinline__ void fill_lut(uint8_t* smem, const uint32_t* lut, int tid, int nthreads) {
   static_assert(REP >= 1 && REP <= 32 && (REP & (REP - 1)) == 0, "REP: power of two");
-  auto entry = [&](int e) {
-    const uint32_t v = __ldg(lut + (e & 511));
-    return (e & 512) ? (v ^ 0x80000000u) : v;
-  };
-  for (int q = tid; q < kLutEntries * REP / 4; q += nthreads) {   // one uint4 = 4 words
-    uint4 u;
-    if constexpr (REP >= 4) {
-      const uint32_t v = entry(q / (REP / 4));
-      u = make_uint4(v, v, v, v);
-    } else {
-      u = make_uint4(entry(4 * q / REP), entry((4 * q + 1) / REP), entry((4 * q + 2) / REP),
-                     entry((4 * q + 3) / REP));
+  if constexpr (REP <= 4) {
+    // entries e, e + 1 (e even) with values a, b: words [e * REP, (e + 2) * REP)
+    auto put = [&](int e, uint32_t a, uint32_t b) {
+      if constexpr (REP == 1) {
+        reinterpret_cast<uint2*>(smem)[e / 2] = make_uint2(a, b);
+      } else if constexpr (REP == 2) {
+        reinterpret_cast<uint4*>(smem)[e / 2] = make_uint4(a, a, b, b);
+      } else {
+        reinterpret_cast<uint4*>(smem)[e] = make_uint4(a, a, a, a);
+        reinterpret_cast<uint4*>(smem)[e + 1] = make_uint4(b, b, b, b);
+      }
+    };
+    for (int t = tid; t < kLutEntries / 4; t += nthreads) {        // 256 source word pairs
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(lut) + t);
+      put(2 * t, v.x, v.y);
+      put(2 * t + kLutEntries / 2, v.x ^ 0x80000000u, v.y ^ 0x80000000u);
     }
-    reinterpret_cast<uint4*>(smem)[q] = u;
+  } else {
+    for (int q = tid; q < kLutEntries * REP / 4; q += nthreads) {  // REP / 4 uint4 per entry
+      const int e = q / (REP / 4);
+      uint32_t v = __ldg(lut + (e & 511));
+      if (e & 512) v ^= 0x80000000u;
+      reinterpret_cast<uint4*>(smem)[q] = make_uint4(v, v, v, v);
+    }
   }
 }
 

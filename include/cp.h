@@ -146,9 +146,10 @@ cp_status cp_table_load_mixed(cp_table** out, const void* records, const uint64_
  *         addressing the host pointer is the device pointer): the kernel then
  *         writes the rows over the host link, with no separate copy.
  * Out-of-range ids give zero rows and set the status word (see cp_get_status).
- * Launch: one kernel of ceil(n / 32) CTAs of 256 threads (32 lookups per CTA),
- * each with 8 KB of LUT plus 32 record stages of shared memory (under 18 KB at
- * d = 1024, b = 2); work from other streams can share the SMs.
+ * Launch (single-rate table): one kernel of ceil(n / 32) CTAs of 256 threads
+ * (32 lookups per CTA), each with 8 KB of LUT plus 32 record stages of shared
+ * memory (under 18 KB at d = 1024, b = 2); work from other streams can share
+ * the SMs.  A mixed-rate table runs one persistent 1024-thread CTA per SM.
  */
 cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                            void* stream);

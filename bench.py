@@ -68,6 +68,8 @@ def parse():
                     help="run one section alone (no table in device memory) and print its JSON")
     ap.add_argument("--encoder-rows", type=int, default=0,
                     help="rows per encoder call (default 4 x SM count)")
+    ap.add_argument("--sustained-calls", type=int, default=50,
+                    help="back-to-back calls in the sustained window (0: skip)")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip timing the other table configs (mid, bit-rate sweep, decode step)")
     return ap.parse_args()
@@ -204,6 +206,71 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def cpu_model() -> str:
+    """Host CPU model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def workload_config(w, layout: str, world: int, idx_np: np.ndarray, index_seed: int) -> dict:
+    """The `config` object of both arms' JSON lines (identical keys and values)."""
+    from trellis_row_decode_gb300 import synth
+    return {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
+            "record_bytes": w.rec_bytes, "lookups": int(idx_np.size), "tokens": w.tokens,
+            "rows_per_token": w.rows_per_token, "index_dist": f"{w.dist}({w.zipf_s})",
+            "unique_ids": int(np.unique(idx_np).size), "layout": layout,
+            "table_gb": w.table_bytes / 1e9,
+            "seeds": {"table": synth.SEED_TABLE, "index": index_seed},
+            "l2": "flushed between steps (512 MB write then 512 MB read, outside the timed interval)",
+            "parallelism": f"replicas x{world}", "cpu_model": cpu_model()}
+
+
+def oracle_parity(w, idx_np: np.ndarray, out_host, lut, chunk: int = 1 << 16) -> dict:
+    """Every element of a timed step's output (bf16 [n, d] on the host) against the
+    oracle's decode of the same lookups (records regenerated on the host).  Part of
+    the CPU-baseline leg: the only place besides --impl reference where the bench
+    runs the oracle."""
+    import torch
+    import oracle
+    from trellis_row_decode_gb300 import synth
+    got_all = out_host.view(torch.int16).numpy().view(np.uint16)
+    n_bad, max_ulp = 0, 0
+    nt = max(1, os.cpu_count() or 1)
+    for j0 in range(0, idx_np.size, chunk):
+        ids = idx_np[j0:j0 + chunk]
+        valid = (ids >= 0) & (ids < w.n_rows)
+        uniq, inv = np.unique(np.where(valid, ids, 0), return_inverse=True)
+        rec = synth.gen_records(synth.SEED_TABLE, torch.from_numpy(uniq), w.d, w.k).numpy()
+        local = np.where(valid, inv, -1).astype(np.int64)
+        ref, _ = oracle.lookup_decode(rec, len(uniq), w.d, w.k, rec.shape[1], lut, local,
+                                      n_threads=nt)
+        got = got_all[j0:j0 + chunk].reshape(ref.shape)
+        if np.array_equal(got, ref):
+            continue
+        g, r = got.astype(np.int32), ref.astype(np.int32)
+        nan = ((g & 0x7FFF) > 0x7F80) & ((r & 0x7FFF) > 0x7F80)
+        diff = (g != r) & ~nan
+        line = lambda x: np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)  # noqa: E731
+        n_bad += int(diff.sum())
+        if diff.any():
+            max_ulp = max(max_ulp, int(np.abs(line(g) - line(r))[diff].max()))
+    return {"checked_elements": int(idx_np.size) * w.d, "deviating": n_bad, "max_ulp": max_ulp,
+            "against": "oracle (every row of the last timed step)"}
+
+
 # ---------------------------------------------------------------------------
 # Reference arm: the CPU oracle on the host cores.
 # ---------------------------------------------------------------------------
@@ -250,8 +317,9 @@ def reference_arm(args, w, rank):
     if rank != 0:
         return
     import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
     lut = cp.default_lut()
-    idx = w.indices()
+    idx = w.indices(synth.SEED_INDEX)
     # the whole run stays near args.cpu_seconds: each step times a prefix sized
     # for its share (at least the 2048-lookup calibration prefix)
     # one calibration, then every step times the same prefix, sized so that the
@@ -273,8 +341,7 @@ def reference_arm(args, w, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * w.n_lookups / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-        "config": {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
-                   "lookups": w.n_lookups, "index_dist": f"{w.dist}({w.zipf_s})"},
+        "config": workload_config(w, args.layout, args.gpus, idx, synth.SEED_INDEX),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nt, "kind": "oracle",
                          "sample": f"first {sizes[0]} lookups of the replay per step (records "
                                    f"regenerated on the host once), {nt} threads"},
@@ -395,6 +462,7 @@ def our_arm(args, w, rank, world, local):
         dist.barrier()
     status = cp.get_status(table)
     assert status == cp.CP_OK, status
+    out_host = out.cpu()                       # the last timed step's rows, for the parity check
     total, value = aggregate(float(t.sum()), n * args.steps, world, dist, "cuda")
     mean_t = total / args.steps
     bpl = w.algorithmic_bytes_per_lookup()
@@ -405,6 +473,9 @@ def our_arm(args, w, rank, world, local):
     # single-GPU characterisation legs run at N = 1 only (they would hold every
     # GPU of a multi-rank job while rank 0 alone works)
     solo = world == 1
+    sustained = None
+    if solo and args.sustained_calls > 0:
+        sustained = sustained_measure(args, w, table, out, flush, stream, bpl=w.algorithmic_bytes_per_lookup())
     ctx = hbm_same_run(flush, stream) if solo else None
     if ctx is not None:
         ctx["decode_frac_of_copy"] = achieved / ctx["copy_gbs"]
@@ -485,7 +556,9 @@ def our_arm(args, w, rank, world, local):
         host_obj = host_path_measure(args, w, idx, flush, stream)
 
     cpu = None
+    parity = None
     if solo and not args.no_cpu_baseline:
+        parity = oracle_parity(w, idx_np, out_host, cp.default_lut())
         rate, m, nt = oracle_sample_rate(w, idx_np, args.cpu_seconds, cp.default_lut())
         rate1, m1, _ = oracle_sample_rate(w, idx_np, args.cpu_seconds / 4, cp.default_lut(), 1)
         cpu = {"value": rate, "unit": "rows/s", "cores": nt, "kind": "oracle",
@@ -503,13 +576,7 @@ def our_arm(args, w, rank, world, local):
             "vs_baseline": value / world / (w.n_lookups / PAGES_LATENCY_S)
             if w.name == "deepseek_prefill" else None,
             "dtype": "fp32", "data": "synthetic",
-            "config": {"workload": w.name, "n_rows": w.n_rows, "d": w.d, "b": w.k / 2,
-                       "record_bytes": w.rec_bytes, "lookups": n, "tokens": w.tokens,
-                       "rows_per_token": w.rows_per_token,
-                       "index_dist": f"{w.dist}({w.zipf_s})", "layout": args.layout,
-                       "table_gb": w.table_bytes / 1e9,
-                       "l2": "flushed between steps (512 MB write then 512 MB read, outside the timed interval)",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(w, args.layout, world, idx_np, synth.SEED_INDEX + rank),
             "achieved_gbs_algorithmic": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
@@ -523,6 +590,10 @@ def our_arm(args, w, rank, world, local):
             "step_ms": {"min": float(t.min() * 1e3), "median": float(np.median(t) * 1e3),
                         "max": float(t.max() * 1e3)},
         }
+        if parity is not None:
+            line["parity"] = parity
+        if sustained is not None:
+            line["sustained"] = sustained
         if cpu is not None:
             line["cpu_baseline"] = cpu
         if ctx is not None:
@@ -543,32 +614,73 @@ def our_arm(args, w, rank, world, local):
         dist.destroy_process_group()
 
 
+def sustained_measure(args, w, table, out, flush, stream, bpl: int):
+    """Back-to-back decode calls with no flush between them, each over its own replay
+    (index seeds SEED_INDEX + i), after one L2 flush: every call pays the write-back
+    of the rows the previous calls left dirty in L2, as in a serving loop.  The rows
+    alternate between two output buffers (each larger than L2)."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    K = args.sustained_calls
+    ids = [torch.from_numpy(w.indices(synth.SEED_INDEX + i)).cuda() for i in range(K)]
+    outs = [out, torch.empty_like(out)]
+    for i in range(min(K, 3)):                                    # warm-up
+        cp.lookup_decode(table, ids[i], outs[i & 1], stream)
+    flush_l2(flush)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(K):
+        cp.lookup_decode(table, ids[i], outs[i & 1], stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert cp.get_status(table) == cp.CP_OK
+    per = a.elapsed_time(b) * 1e-3 / K
+    n = ids[0].numel()
+    peak = measured_peaks()[0]
+    del outs[1]
+    return {"calls": K, "ms_per_step": per * 1e3, "rows_per_s": n / per,
+            "achieved_gbs": n * bpl / per / 1e9, "frac": n * bpl / per / 1e9 / peak,
+            "replays": f"index seeds {synth.SEED_INDEX}..{synth.SEED_INDEX + K - 1}, one per call",
+            "l2": "flushed once before the window; no flush between calls"}
+
+
 def encoder_measure(args, w):
-    """cp_encode_rows on N(0,1) rows of the workload's d and rate: one warm-up call
-    on half the rows, then one timed call (host clock around call + sync)."""
+    """cp_encode_rows_ws on N(0,1) rows of the workload's d and rate: the workspace
+    is allocated once outside the timing; one warm-up call on half the rows, then
+    one call timed with CUDA events on the launching stream (LUT copy + kernel)."""
     import torch
     import trellis_row_decode_gb300 as cp
     from trellis_row_decode_gb300 import synth
     erows = args.encoder_rows or 4 * torch.cuda.get_device_properties(0).multi_processor_count
     e_in = torch.from_numpy(synth.normal_rows(synth.SEED_ENCODER_ROWS, erows, w.d)
                             .astype(np.float32)).cuda()
-    cp.encode_rows(e_in[: max(1, erows // 2)], w.k)
+    ws = cp.encode_workspace(erows, w.d, w.k)
+    rec = torch.empty((erows, w.rec_bytes), dtype=torch.uint8, device="cuda")
+    ecost = torch.empty(erows, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    half = max(1, erows // 2)
+    cp.encode_rows_ws(e_in[:half], w.k, ws, rec[:half], ecost[:half], stream=stream)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    _, ecost = cp.encode_rows(e_in, w.k)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    cp.encode_rows_ws(e_in, w.k, ws, rec, ecost, stream=stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    et = time.perf_counter() - t0
-    res = {"entry_point": "cp_encode_rows", "rows": erows, "d": w.d, "b": w.k / 2,
+    et = a.elapsed_time(b) * 1e-3
+    res = {"entry_point": "cp_encode_rows_ws", "rows": erows, "d": w.d, "b": w.k / 2,
            "seconds": et, "rows_per_s": erows / et,
-           "mean_cost_per_coord": float(ecost.mean()) / w.d}
+           "mean_cost_per_coord": float(ecost.mean()) / w.d,
+           "timing": "CUDA events on the launching stream around the queued LUT copy and "
+                     "kernel; workspace allocated once before"}
     ipr = ncu_encoder_inst_per_row(w.d, w.k)
     if ipr is not None:
         res["roofline"] = {"bound": "alu", "achieved": ipr * erows / et,
                            "peak": ISSUE_PEAK_WARP_INST_S, "unit": "warp-inst/s",
                            "frac": ipr * erows / et / ISSUE_PEAK_WARP_INST_S,
                            "peak_kind": "derived: 152 SMs x 4 schedulers x 2.07 GHz",
-                           "inst_per_row": ipr,
-                           "note": "call time on the host clock (workspace allocation included)"}
+                           "inst_per_row": ipr}
     return res
 
 
@@ -660,11 +772,18 @@ def host_path_measure(args, w, idx, flush, stream):
             synth.gen_records(synth.SEED_TABLE, rows, w.d, w.k))
         host[r0 * R: r1 * R].copy_(stage[: (r1 - r0) * R])
     torch.cuda.synchronize()
-    # measured host-to-device bandwidth: 1 GB copies from pinned memory
+    # measured host link: 1 GB copies from pinned memory (copy engines), and the
+    # same 1 GB read zero-copy by a streaming kernel on the SMs (the decode's own
+    # access path); the larger of the two is the roofline
     dst = stage[: 1 << 30]
     src = host[: 1 << 30]
     th = time_steps(lambda: dst.copy_(src, non_blocking=True), 10, 2, flush, stream)
     h2d = (1 << 30) / float(np.median(th)) / 1e9
+    tz = time_steps(lambda: cp.measure_stream_read(src, stream), 10, 2, flush, stream)
+    zero_copy = (1 << 30) / float(np.median(tz)) / 1e9
+    link = max(h2d, zero_copy)
+    link_kind = ("zero-copy streaming read of 1 GB pinned (cp_measure_stream_read)"
+                 if zero_copy >= h2d else "cudaMemcpyAsync pinned->device, 1 GB")
     del stage, dst
     table = cp.load_table(host, w.n_rows, w.d, w.k, cp.default_lut())
     n = idx.numel()
@@ -684,17 +803,23 @@ def host_path_measure(args, w, idx, flush, stream):
         assert cp.get_status(table) == cp.CP_OK
         tcm = float(np.median(tc))
         cached = {"hot_rows": 1 << 20, "cache_bytes": (1 << 20) * R, "ms_per_step": tcm * 1e3,
-                  "rows_per_s": n / tcm, "record_gbs": n * R / tcm / 1e9,
-                  "frac_of_h2d": n * R / tcm / 1e9 / h2d}
+                  "rows_per_s": n / tcm,
+                  "lookup_record_gbs": n * R / tcm / 1e9,
+                  "note": "cached ids are read from HBM, so no link fraction applies"}
     table.close()
     return {"entry_point": "cp_lookup_decode_host", "table": "pinned host DRAM",
             "with_hot_row_cache": cached,
             "ms_per_step": tm * 1e3, "rows_per_s": n / tm,
-            "bound": "host link", "achieved": link_gbs, "unit": "GB/s",
-            "peak": h2d, "peak_kind": "measured (cudaMemcpyAsync pinned->device, 1 GB)",
-            "frac": link_gbs / h2d,
-            "bytes_per_lookup": R, "unique_ids": uniq,
-            "unique_record_gbs": uniq * R / tm / 1e9}
+            "bound": "host link", "unit": "GB/s",
+            "link_peak": link, "link_peak_kind": f"measured: {link_kind}",
+            "h2d_memcpy_gbs": h2d, "zero_copy_read_gbs": zero_copy,
+            "unique_ids": uniq, "bytes_per_lookup": R,
+            "achieved_unique": uniq * R / tm / 1e9,
+            "link_frac_unique": uniq * R / tm / 1e9 / link,
+            "achieved_lookup_bytes": link_gbs,
+            "frac_lookup_bytes": link_gbs / link,
+            "note": "link_frac_unique counts the records that cross the link (one per distinct "
+                    "id); frac_lookup_bytes counts n * R as the survey's algorithmic bytes"}
 
 
 def main():

@@ -94,7 +94,9 @@ uint64_t cp_soa_bytes(uint64_t n_rows, uint32_t d, uint32_t bits_per_step);
  * for CP_LAYOUT_SOA, repack the records on the device into `soa_dst`.
  *
  *   out           receives the handle (set to NULL on error).
- *   records       AoS records, n_rows * R bytes, 16-byte aligned.
+ *   records       AoS records, n_rows * R bytes, 16-byte aligned.  The buffer
+ *                 must span all n_rows * R bytes: the kernels read up to its
+ *                 last byte and this call cannot check the size of a pointer.
  *                 CP_RESIDENT_DEVICE: device memory.
  *                 CP_RESIDENT_HOST: host memory, page-locked by the caller
  *                 (cudaHostAlloc, or cudaHostRegister).  If it is plain pageable
@@ -240,6 +242,30 @@ cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d, uint32_t bit
                          const uint16_t* lut_fp16, uint8_t* records, float* cost, void* stream);
 
 /*
+ * cp_encode_workspace_bytes -- device workspace that cp_encode_rows_ws needs for
+ * `rows` rows of this geometry on the current device (traceback bytes of every
+ * cluster in flight plus 2 KB for the LUT); 0 for a rejected geometry or when
+ * the device cannot run the encoder's clusters.
+ */
+uint64_t cp_encode_workspace_bytes(uint64_t rows, uint32_t d, uint32_t bits_per_step);
+
+/*
+ * cp_encode_rows_ws -- cp_encode_rows with a caller-owned workspace: it queues
+ * the LUT copy and the encoder kernel on `stream` and returns without
+ * synchronising or allocating, so the kernel can be timed with events and
+ * repeated calls reuse one workspace.  Same arguments and results as
+ * cp_encode_rows, plus
+ *   workspace        device memory, 256-byte aligned, at least
+ *                    cp_encode_workspace_bytes(rows, d, bits_per_step) bytes;
+ *                    used until the queued work completes (calls sharing it
+ *                    must be ordered on one stream).
+ *   workspace_bytes  its size; CP_ERR_INVALID_ARG when too small.
+ */
+cp_status cp_encode_rows_ws(const float* e, uint64_t rows, uint32_t d, uint32_t bits_per_step,
+                            const uint16_t* lut_fp16, uint8_t* records, float* cost,
+                            void* workspace, uint64_t workspace_bytes, void* stream);
+
+/*
  * cp_get_status -- synchronise `stream`, then report and clear the table's
  * device status word: CP_ERR_INDEX_OOB if any decode since the last call saw an
  * out-of-range id, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK.
@@ -257,7 +283,9 @@ cp_status cp_get_status(const cp_table* t, void* stream);
  * device), or a runtime that fixes its memory budget up front.  cp_table_load
  * allocates, so such callers pass everything themselves:
  *   records   pinned, mapped host memory holding n_rows AoS records (16-byte
- *             aligned; page-locked by the caller, e.g. cudaHostAlloc).
+ *             aligned; page-locked by the caller, e.g. cudaHostAlloc).  It must
+ *             span n_rows * R bytes: the kernels may read up to its last byte
+ *             over the host link, and the library cannot check the size.
  *   n_rows, d, bits_per_step: geometry as for cp_table_load.
  *   lut_fp16  host pointer, 512 x (y0, y1) fp16 patterns, finite.
  *   idx       device, n int64 ids;  out: device bf16 [n][d], 16-byte aligned.
@@ -268,7 +296,9 @@ cp_status cp_get_status(const cp_table* t, void* stream);
  * library holds until the process exits.  Limit: n <= 65536 lookups per call;
  * larger n returns CP_ERR_INVALID_ARG before any work is queued.
  * The first call on a device looks up that array's device address (once per
- * device); make that first call before any stream capture.  All calls share the
+ * device); make that first call before any stream capture.  The address is kept
+ * for the life of the process: after cudaDeviceReset it no longer names the
+ * array, so do not call this entry point on a device that has been reset.  All calls share the
  * array and it keeps the last call's contents (each call clears what must start
  * empty), so calls that overlap on the GPU (on different streams, or from
  * different threads without ordering) race: order them on one stream.
@@ -278,6 +308,22 @@ cp_status cp_lookup_decode_host_noalloc(const void* records, uint64_t n_rows, ui
                                         uint32_t bits_per_step, const uint16_t* lut_fp16,
                                         const int64_t* idx, uint64_t n, uint16_t* out,
                                         uint32_t* status, void* stream);
+
+/*
+ * cp_measure_stream_read -- read `bytes` bytes of `buf` once with a streaming
+ * kernel (16-byte loads, grid-stride, four loads in flight per thread; nothing
+ * observable is written).  Timed with events on `stream`, it gives the
+ * bandwidth that bounds a lookup-decode: read zero-copy from page-locked host
+ * memory it is the host link's rate (the roofline of cp_lookup_decode_host,
+ * beside a cudaMemcpyAsync from the same memory); from device memory it is the
+ * HBM read rate.  The pages give the host link only as the path of the slow
+ * placement [P4 "assumptions and limits"]; this measures it on the machine.
+ *   buf    device memory, or page-locked host memory the device can address;
+ *          16-byte aligned.
+ *   bytes  a positive multiple of 16.
+ * CP_ERR_INVALID_ARG for any other buffer; queues one kernel, no allocation.
+ */
+cp_status cp_measure_stream_read(const void* buf, uint64_t bytes, void* stream);
 
 /* Release what the handle owns (LUT copy, status word, host registration made
  * by cp_table_load).  Borrowed buffers are untouched.  NULL is a no-op. */

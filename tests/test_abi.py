@@ -96,3 +96,24 @@ def test_bad_arguments_rejected_on_host(cplib):
     cplib.cp_table_free(None)
     assert cplib.cp_test_inject_failure(9, 1) == 1
     assert np.isfinite(lut.view(np.float16).astype(float)).all()
+
+
+def test_wrappers_reject_short_record_buffers(cplib):
+    """A records buffer shorter than n_rows * R would let the kernels read past its
+    end (the C ABI only sees a pointer), so the binding refuses it before any call
+    into the library; the same for a short SoA destination."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    d, k, n_rows = 256, 4, 100
+    R = cp.record_bytes(d, k)
+    short = torch.zeros(n_rows * R - 2, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        cp.load_table(short, n_rows, d, k)
+    with pytest.raises(ValueError):
+        cp.lookup_decode_host_noalloc(short, n_rows, d, k, torch.zeros(1, dtype=torch.int64),
+                                      torch.empty((1, d), dtype=torch.bfloat16),
+                                      torch.zeros(1, dtype=torch.int32))
+    full = torch.zeros(n_rows * R, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        cp.load_table(full, n_rows, d, k, layout=cp.CP_LAYOUT_SOA,
+                      soa=torch.zeros(cp.soa_bytes(n_rows, d, k) - 16, dtype=torch.uint8))

@@ -2,8 +2,8 @@
 allocate device memory (its scratch is a static device array inside libcp).
 
 Collected last on purpose.  It must agree bit for bit with cp_lookup_decode_host
-(the tolerance of every parity test here), on two calls in a row that share the
-static scratch, whether run alone or after the other tests.
+and with the oracle (the tolerance of every parity test here), on two calls in a
+row that share the static scratch, whether run alone or after the other tests.
 """
 import ctypes as C
 
@@ -13,6 +13,8 @@ import torch
 
 import trellis_row_decode_gb300 as cp
 from trellis_row_decode_gb300 import synth
+
+from gpu_util import compare, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +45,9 @@ def test_noalloc_matches_table_entry_point_on_consecutive_calls():
         if call == 1:
             assert torch.cuda.mem_get_info()[0] >= free_before - (2 << 20)
         assert np.array_equal(_bits(out), _bits(ref)), f"call {call}: output differs"
+        n_bad, ulp = compare(_bits(out).view(np.uint16),
+                             oracle_decode(11, d, k, idx_np, n_rows, cp.default_lut()))
+        assert n_bad == 0, f"call {call}: {n_bad} elements differ from the oracle ({ulp} ulp)"
         assert int(status.item()) & 1 == 1
         assert not out[3].view(torch.int16).any()
     table.close()
@@ -63,3 +68,14 @@ def test_noalloc_rejects_more_than_its_capacity():
     assert b"65536" in cp.lib().cp_last_error()
     torch.cuda.synchronize()
     assert bool((out.float() == 3.0).all())              # nothing was queued
+
+
+def test_noalloc_rejects_a_short_records_buffer():
+    """The wrapper refuses a pinned buffer smaller than n_rows records, before any launch."""
+    d, k, n_rows = 256, 4, 100
+    rec = torch.zeros(n_rows * synth.record_bytes(d, k) - 2, dtype=torch.uint8).pin_memory()
+    idx = torch.zeros(4, dtype=torch.int64, device="cuda")
+    out = torch.empty((4, d), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        cp.lookup_decode_host_noalloc(rec, n_rows, d, k, idx, out, status)

@@ -23,6 +23,7 @@ __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
     "lookup_decode_reduce", "set_cache", "load_mixed_table", "encode_rows",
+    "measure_stream_read", "encode_workspace", "encode_rows_ws",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -84,6 +85,12 @@ def lib():
         L.cp_lookup_decode_reduce.argtypes = [vp, vp, u64, u32, vp, vp, vp]
         L.cp_lookup_decode_host_noalloc.restype = i32
         L.cp_lookup_decode_host_noalloc.argtypes = [vp, u64, u32, u32, vp, vp, u64, vp, vp, vp]
+        L.cp_encode_workspace_bytes.restype = u64
+        L.cp_encode_workspace_bytes.argtypes = [u64, u32, u32]
+        L.cp_encode_rows_ws.restype = i32
+        L.cp_encode_rows_ws.argtypes = [vp, u64, u32, u32, vp, vp, vp, vp, u64, vp]
+        L.cp_measure_stream_read.restype = i32
+        L.cp_measure_stream_read.argtypes = [vp, u64, vp]
         _lib = L
     return _lib
 
@@ -134,6 +141,15 @@ class Table:
             pass
 
 
+def _check_span(records: torch.Tensor, n_rows: int, d: int, k: int) -> None:
+    """The kernels read up to n_rows * R bytes of `records` (R = record_bytes(d, k)),
+    which the C ABI cannot check: refuse a shorter buffer before anything is queued."""
+    R = record_bytes(d, k)
+    if R and n_rows > 0 and records.numel() < n_rows * R:
+        raise ValueError(f"records holds {records.numel()} bytes, fewer than n_rows * R = "
+                         f"{n_rows} * {R}")
+
+
 def load_table(records: torch.Tensor, n_rows: int, d: int, k: int, lut: np.ndarray | None = None,
                layout: int = CP_LAYOUT_AOS, soa: torch.Tensor | None = None,
                stream=None) -> Table:
@@ -147,6 +163,7 @@ def load_table(records: torch.Tensor, n_rows: int, d: int, k: int, lut: np.ndarr
     if records.dtype != torch.uint8 or not records.is_contiguous():
         raise ValueError("records must be a contiguous uint8 tensor")
     residency = CP_RESIDENT_DEVICE if records.is_cuda else CP_RESIDENT_HOST
+    _check_span(records, n_rows, d, k)
     if lut is None:
         lut = default_lut()
     lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
@@ -155,6 +172,10 @@ def load_table(records: torch.Tensor, n_rows: int, d: int, k: int, lut: np.ndarr
     if layout == CP_LAYOUT_SOA:
         if soa is None:
             raise ValueError("CP_LAYOUT_SOA needs the soa buffer")
+        if soa.dtype != torch.uint8 or not soa.is_contiguous() or soa.is_cuda != records.is_cuda \
+                or soa.numel() < soa_bytes(n_rows, d, k):
+            raise ValueError("soa must be a contiguous uint8 tensor of soa_bytes(n_rows, d, k) "
+                             "bytes on the records' side (device or pinned host)")
         soa_ptr = soa.data_ptr()
     st = L.cp_table_load(C.byref(h), records.data_ptr(), n_rows, d, k,
                          lut.ctypes.data, residency, layout, soa_ptr, _stream_ptr(stream))
@@ -172,6 +193,10 @@ def load_mixed_table(records: torch.Tensor, offsets: torch.Tensor, d: int,
     if lut is None:
         lut = default_lut()
     lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    if not offsets.is_contiguous() or not records.is_contiguous() or offsets.numel() < 2:
+        raise ValueError("records and offsets must be contiguous, offsets of n_rows + 1 entries")
+    if int(offsets[-1].item()) > records.numel():
+        raise ValueError("offsets[n_rows] exceeds the bytes held by records")
     h = C.c_void_p(0)
     n_rows = offsets.numel() - 1
     st = lib().cp_table_load_mixed(C.byref(h), records.data_ptr(), offsets.data_ptr(), n_rows, d,
@@ -242,6 +267,9 @@ def set_cache(table: Table, hot_rows, cache: torch.Tensor | None = None, stream=
     m = rows.size
     if m and cache is None:
         cache = torch.empty(m * record_bytes(table.d, table.k), dtype=torch.uint8, device="cuda")
+    if m and (not cache.is_cuda or cache.dtype != torch.uint8 or not cache.is_contiguous()
+              or cache.numel() < m * record_bytes(table.d, table.k)):
+        raise ValueError("cache must be a contiguous uint8 CUDA tensor of len(hot_rows) * R bytes")
     ptr = cache.data_ptr() if m else None
     _check(lib().cp_table_set_cache(table.handle, rows.ctypes.data if m else None, m, ptr,
                                     _stream_ptr(stream)), "cp_table_set_cache")
@@ -264,6 +292,46 @@ def encode_rows(e: torch.Tensor, k: int, lut: np.ndarray | None = None, stream=N
     return rec, cost
 
 
+def measure_stream_read(buf: torch.Tensor, stream=None) -> None:
+    """Queue one streaming read of all of `buf` (device memory, or pinned host memory
+    read zero-copy over the host link); time it with events on `stream`."""
+    if not buf.is_contiguous() or (buf.numel() * buf.element_size()) % 16:
+        raise ValueError("buf must be contiguous with a size that is a multiple of 16 bytes")
+    _check(lib().cp_measure_stream_read(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                        _stream_ptr(stream)), "cp_measure_stream_read")
+
+
+def encode_workspace(rows: int, d: int, k: int) -> torch.Tensor:
+    """A device workspace for encode_rows_ws (uint8, cp_encode_workspace_bytes bytes)."""
+    nb = int(lib().cp_encode_workspace_bytes(rows, d, k))
+    if nb == 0:
+        raise CPError(CP_ERR_INVALID_ARG, "cp_encode_workspace_bytes")
+    return torch.empty(nb, dtype=torch.uint8, device="cuda")
+
+
+def encode_rows_ws(e: torch.Tensor, k: int, workspace: torch.Tensor, records: torch.Tensor,
+                   cost: torch.Tensor | None = None, lut: np.ndarray | None = None,
+                   stream=None) -> None:
+    """encode_rows into caller buffers with a caller-owned workspace; only queues work
+    on `stream` (no synchronisation, no allocation)."""
+    if not e.is_cuda or e.dtype != torch.float32 or e.dim() != 2 or not e.is_contiguous():
+        raise ValueError("e must be a contiguous 2-D float32 CUDA tensor")
+    rows, d = e.shape
+    if records.dtype != torch.uint8 or not records.is_cuda or not records.is_contiguous() \
+            or records.numel() < rows * record_bytes(d, k):
+        raise ValueError("records must be a contiguous uint8 CUDA tensor of rows * R bytes")
+    if cost is not None and (cost.dtype != torch.float32 or not cost.is_cuda
+                             or cost.numel() < rows):
+        raise ValueError("cost must be a float32 CUDA tensor of one value per row")
+    if lut is None:
+        lut = default_lut()
+    lut = np.ascontiguousarray(lut, dtype=np.uint16).reshape(512, 2)
+    _check(lib().cp_encode_rows_ws(e.data_ptr(), rows, d, k, lut.ctypes.data, records.data_ptr(),
+                                   cost.data_ptr() if cost is not None else None,
+                                   workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
+           "cp_encode_rows_ws")
+
+
 def get_status(table: Table, stream=None) -> int:
     """Synchronise the stream; CP_ERR_INDEX_OOB if an id was out of range since the last call."""
     return int(lib().cp_get_status(table.handle, _stream_ptr(stream)))
@@ -282,6 +350,7 @@ def lookup_decode_host_noalloc(records: torch.Tensor, n_rows: int, d: int, k: in
     """
     if records.is_cuda or records.dtype != torch.uint8 or not records.is_contiguous():
         raise ValueError("records must be a contiguous pinned uint8 host tensor")
+    _check_span(records, n_rows, d, k)
     if idx.dtype != torch.int64 or not idx.is_cuda or not idx.is_contiguous():
         raise ValueError("idx must be a contiguous int64 CUDA tensor")
     if out.dtype != torch.bfloat16 or out.shape != (idx.numel(), d) or not out.is_contiguous():

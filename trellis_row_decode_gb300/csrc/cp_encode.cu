@@ -569,11 +569,22 @@ EncodeFn encode_kernel(uint32_t k) {
 
 }  // namespace cpk
 
-extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
-                                    uint32_t bits_per_step, const uint16_t* lut_fp16,
-                                    uint8_t* records, float* cost, void* stream) {
+namespace {
+
+// Launch configuration shared by the encoder entry points: the kernel, its
+// shared memory, the clusters in flight for `rows` rows and the traceback
+// bytes per cluster.
+struct EncLaunch {
+  cpk::EncodeFn fn;
+  cpk::EncSmem smem;
+  uint64_t clusters;
+  uint64_t stride;
+};
+
+cp_status enc_args_ok(const float* e, uint64_t rows, uint32_t d, uint32_t k,
+                      const uint16_t* lut_fp16, const uint8_t* records, const float* cost) {
   if (e == nullptr || records == nullptr || lut_fp16 == nullptr || rows == 0 ||
-      !cpx::geometry_ok(d, bits_per_step) || d < 16 || !cpx::aligned(e, 4) ||
+      !cpx::geometry_ok(d, k) || d < 16 || !cpx::aligned(e, 4) ||
       (cost != nullptr && !cpx::aligned(cost, 4))) {
     cpx::set_error("bad rows/records/LUT pointer or geometry");
     return CP_ERR_INVALID_ARG;
@@ -584,44 +595,75 @@ extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
       return CP_ERR_FORMAT;
     }
   }
-  const uint32_t k = bits_per_step, T = d / 2, W = 16 - k;
-  const cpk::EncSmem L = cpk::enc_smem(d, k);
-  cpk::EncodeFn fn = cpk::encode_kernel(k);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+  return CP_OK;
+}
+
+cp_status enc_launch_config(uint64_t rows, uint32_t d, uint32_t k, EncLaunch* out,
+                            cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr) {
+  const uint32_t T = d / 2, W = 16 - k;
+  out->smem = cpk::enc_smem(d, k);
+  out->fn = cpk::encode_kernel(k);
+  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(out->fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(L.total));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+                                         static_cast<int>(out->smem.total));
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cpk::kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(cpk::kEncThreads);
-  cfg.dynamicSmemBytes = L.total;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  *cfg = cudaLaunchConfig_t{};
+  cfg->blockDim = dim3(cpk::kEncThreads);
+  cfg->dynamicSmemBytes = out->smem.total;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
   int max_clusters = 0;
   if (err == cudaSuccess) {
-    cfg.gridDim = dim3(cpk::kCluster * 64);
-    err = cudaOccupancyMaxActiveClusters(&max_clusters, reinterpret_cast<const void*>(fn), &cfg);
+    cfg->gridDim = dim3(cpk::kCluster * 64);
+    err = cudaOccupancyMaxActiveClusters(&max_clusters, reinterpret_cast<const void*>(out->fn),
+                                         cfg);
   }
   if (err != cudaSuccess || max_clusters < 1) {
     if (err == cudaSuccess) err = cudaErrorInvalidConfiguration;
     return cpx::cuda_fail(err, "tcq encoder cluster occupancy");
   }
-  const uint64_t clusters =
+  out->clusters =
       rows < static_cast<uint64_t>(max_clusters) ? rows : static_cast<uint64_t>(max_clusters);
-  const uint64_t stride = (static_cast<uint64_t>(T) * (1ull << W) + 255) & ~255ull;
-  void* mem = nullptr;
-  err = cudaMalloc(&mem, clusters * stride + 2048);
-  if (err != cudaSuccess) {
-    cpx::cuda_fail(err, "cudaMalloc(encoder workspace)");
-    return CP_ERR_NO_MEMORY;
+  out->stride = (static_cast<uint64_t>(T) * (1ull << W) + 255) & ~255ull;
+  cfg->gridDim = dim3(static_cast<unsigned>(out->clusters * cpk::kCluster));
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" uint64_t cp_encode_workspace_bytes(uint64_t rows, uint32_t d, uint32_t bits_per_step) {
+  if (rows == 0 || !cpx::geometry_ok(d, bits_per_step) || d < 16) return 0;
+  EncLaunch el;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  if (enc_launch_config(rows, d, bits_per_step, &el, &cfg, attr) != CP_OK) return 0;
+  return el.clusters * el.stride + 2048;
+}
+
+extern "C" cp_status cp_encode_rows_ws(const float* e, uint64_t rows, uint32_t d,
+                                       uint32_t bits_per_step, const uint16_t* lut_fp16,
+                                       uint8_t* records, float* cost, void* workspace,
+                                       uint64_t workspace_bytes, void* stream) {
+  cp_status st = enc_args_ok(e, rows, d, bits_per_step, lut_fp16, records, cost);
+  if (st != CP_OK) return st;
+  EncLaunch el;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  st = enc_launch_config(rows, d, bits_per_step, &el, &cfg, attr);
+  if (st != CP_OK) return st;
+  if (workspace == nullptr || !cpx::aligned(workspace, 256) ||
+      workspace_bytes < el.clusters * el.stride + 2048) {
+    cpx::set_error("workspace must be 256-byte aligned and hold cp_encode_workspace_bytes bytes");
+    return CP_ERR_INVALID_ARG;
   }
-  uint32_t* lut_dev = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mem) + clusters * stride);
-  err = cudaMemcpyAsync(lut_dev, lut_fp16, 2048, cudaMemcpyHostToDevice, s);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cfg.stream = s;
+  uint32_t* lut_dev =
+      reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + el.clusters * el.stride);
+  cudaError_t err = cudaMemcpyAsync(lut_dev, lut_fp16, 2048, cudaMemcpyHostToDevice, s);
   cpk::EncodeParams p;
   p.e = e;
   p.rows = rows;
@@ -629,14 +671,31 @@ extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
   p.lut = lut_dev;
   p.records = records;
   p.cost = cost;
-  p.work = static_cast<uint8_t*>(mem);
-  p.work_stride = stride;
-  if (err == cudaSuccess) {
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cpk::kCluster));
-    err = cudaLaunchKernelEx(&cfg, fn, p);
-  }
-  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
-  cudaFree(mem);
+  p.work = static_cast<uint8_t*>(workspace);
+  p.work_stride = el.stride;
+  if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, el.fn, p);
   if (err != cudaSuccess) return cpx::cuda_fail(err, "tcq encoder");
   return CP_OK;
+}
+
+extern "C" cp_status cp_encode_rows(const float* e, uint64_t rows, uint32_t d,
+                                    uint32_t bits_per_step, const uint16_t* lut_fp16,
+                                    uint8_t* records, float* cost, void* stream) {
+  cp_status st = enc_args_ok(e, rows, d, bits_per_step, lut_fp16, records, cost);
+  if (st != CP_OK) return st;
+  const uint64_t bytes = cp_encode_workspace_bytes(rows, d, bits_per_step);
+  if (bytes == 0) return CP_ERR_CUDA;                   // occupancy query failed (error set)
+  void* mem = nullptr;
+  cudaError_t err = cudaMalloc(&mem, bytes);
+  if (err != cudaSuccess) {
+    cpx::cuda_fail(err, "cudaMalloc(encoder workspace)");
+    return CP_ERR_NO_MEMORY;
+  }
+  st = cp_encode_rows_ws(e, rows, d, bits_per_step, lut_fp16, records, cost, mem, bytes, stream);
+  if (st == CP_OK) {
+    err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) st = cpx::cuda_fail(err, "tcq encoder");
+  }
+  cudaFree(mem);
+  return st;
 }

@@ -102,6 +102,10 @@ def lib():
         L.orc_encode_rows_f32.restype = C.c_int
         L.orc_encode_rows_f32.argtypes = [f32p, C.c_uint64, C.c_uint32, C.c_uint32, u16p, C.c_int,
                                           u8p, f32p]
+        L.orc_free_start_f.restype = C.c_float
+        L.orc_free_start_f.argtypes = [f32p, C.c_uint32, C.c_uint32, u16p, C.c_uint32, u32p]
+        L.orc_free_start_brute_f.restype = C.c_float
+        L.orc_free_start_brute_f.argtypes = [f32p, C.c_uint32, C.c_uint32, u16p, C.c_uint32, u32p]
         L.orc_rtn2.restype = None
         L.orc_rtn2.argtypes = [f64p, C.c_uint32, C.c_int, f64p]
     return _lib
@@ -292,6 +296,22 @@ def encode_z_f32(z: np.ndarray, d: int, k: int, lut: np.ndarray, mode: int):
     if cost < 0:
         raise ValueError("search mode does not apply to this geometry")
     return code, cost
+
+
+def free_start_f32(z: np.ndarray, d: int, k: int, lut: np.ndarray, rho: int | None = None,
+                   brute: bool = False):
+    """First pass of the two-pass search (test hook): free-start fp32 Viterbi over the
+    steps in the order rho, rho + 1, ... (mod T; default rho = T/2).  Returns (cost,
+    states of the best path at each original step).  brute=True: the same minimum by
+    enumerating every path (small T only)."""
+    T = d // 2
+    rho = T // 2 if rho is None else rho
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    lut = np.ascontiguousarray(lut, dtype=np.uint16)
+    states = np.zeros(T, dtype=np.uint32)
+    fn = lib().orc_free_start_brute_f if brute else lib().orc_free_start_f
+    cost = fn(_p(z, C.c_float), d, k, _p(lut, C.c_uint16), rho, _p(states, C.c_uint32))
+    return cost, states
 
 
 def encode_rows_f32(e: np.ndarray, d: int, k: int, lut: np.ndarray,

@@ -29,6 +29,7 @@
 // no multiply-add is fused.
 
 #include <cmath>
+#include <functional>
 #include <cstdint>
 #include <cstring>
 #include <limits>
@@ -559,6 +560,59 @@ float viterbi_two_pass_f(const float* z, const Geometry& g, const StateTableF& s
   return viterbi_fixed_w_f(z, g, st, s >> k, code_out);
 }
 
+// The first pass of the two-pass search on its own (a test hook): a free-start
+// fp32 Viterbi over the steps taken in the order rho, rho + 1, ... (mod T), every
+// state live at the start.  Returns the best final metric (ties to the smaller
+// state) and writes the states of that best path at every original step t.
+// Any tail-biting code is one of these paths, so its result never exceeds the
+// exact tail-biting cost (a relaxation).
+float free_start_f(const float* z, const Geometry& g, const StateTableF& st, uint32_t rho,
+                   uint32_t* states) {
+  const uint32_t k = g.k, T = g.T, W = kStateBits - k, groups = 1u << W;
+  std::vector<float> cur(kStates);
+  for (uint32_t s = 0; s < kStates; ++s) cur[s] = step_cost_f(st, z, rho % T, s);
+  std::vector<uint8_t> tb;
+  const std::vector<float> fin = viterbi_pass_f(z, g, st, cur, rho, -1, tb);
+  const int64_t best = argmin_state_f(fin);
+  uint32_t s = (uint32_t)best;
+  for (int64_t i = T - 1; i >= 0; --i) {
+    states[(rho + (uint32_t)i) % T] = s;
+    if (i > 0) {
+      const uint32_t grp = s & (groups - 1);
+      s = (grp << k) | tb[(size_t)i * groups + grp];
+    }
+  }
+  return fin[best];
+}
+
+// The same minimum by enumeration (a test hook for small T): every start state
+// and every k-bit symbol at each later step, the cost of a path accumulated in
+// fp32 in the pass's step order, the first strictly smaller cost kept.
+float free_start_brute_f(const float* z, const Geometry& g, const StateTableF& st, uint32_t rho,
+                         uint32_t* states) {
+  const uint32_t k = g.k, T = g.T, W = kStateBits - k;
+  std::vector<uint32_t> path(T), best_path(T);
+  float best = std::numeric_limits<float>::infinity();
+  std::function<void(uint32_t, uint32_t, float)> extend = [&](uint32_t i, uint32_t s, float acc) {
+    path[i] = s;
+    if (i + 1 == T) {
+      if (acc < best) {
+        best = acc;
+        best_path = path;
+      }
+      return;
+    }
+    const uint32_t t = (rho + i + 1) % T;
+    for (uint32_t x = 0; x < (1u << k); ++x) {
+      const uint32_t ns = (s >> k) | (x << W);
+      extend(i + 1, ns, acc + step_cost_f(st, z, t, ns));
+    }
+  };
+  for (uint32_t s0 = 0; s0 < kStates; ++s0) extend(0, s0, step_cost_f(st, z, rho % T, s0));
+  for (uint32_t i = 0; i < T; ++i) states[(rho + i) % T] = best_path[i];
+  return best;
+}
+
 float brute_force_f(const float* z, const Geometry& g, const StateTableF& st, uint8_t* code_out) {
   const size_t nb = (g.Lc + 7) / 8;
   std::vector<uint8_t> code(nb);
@@ -943,6 +997,16 @@ float orc_encode_z_f32(const float* z, uint32_t d, uint32_t k, const uint16_t* l
 // alpha = nrm / sqrt(sum f^2) (fp64, index order) rounded once to bf16; a zero
 // row gets an all-zero code and alpha = 0.  cost (optional) receives the fp32
 // path metric.
+float orc_free_start_f(const float* z, uint32_t d, uint32_t k, const uint16_t* lut, uint32_t rho,
+                       uint32_t* states) {
+  return free_start_f(z, make_geometry(d, k), make_state_table_f(lut), rho, states);
+}
+
+float orc_free_start_brute_f(const float* z, uint32_t d, uint32_t k, const uint16_t* lut,
+                             uint32_t rho, uint32_t* states) {
+  return free_start_brute_f(z, make_geometry(d, k), make_state_table_f(lut), rho, states);
+}
+
 int orc_encode_rows_f32(const float* e, uint64_t rows, uint32_t d, uint32_t k, const uint16_t* lut,
                         int n_threads, uint8_t* records, float* cost) {
   const Geometry g = make_geometry(d, k);

@@ -64,8 +64,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["encoder"], default=None,
-                    help="run one section alone (no table in device memory) and print its JSON")
+    ap.add_argument("--only", choices=["encoder", "decode", "host", "mixed", "reduce"],
+                    default=None,
+                    help="run one leg alone on --workload and print its JSON (profiling)")
+    ap.add_argument("--mixed-rows", type=int, default=1 << 24,
+                    help="rows of the mixed-rate table (mixed leg)")
     ap.add_argument("--encoder-rows", type=int, default=0,
                     help="rows per encoder call (default 4 x SM count)")
     ap.add_argument("--sustained-calls", type=int, default=50,
@@ -483,53 +486,11 @@ def our_arm(args, w, rank, world, local):
         others = other_configs(args, w, table, idx, out, flush, stream)
 
     # Decode fused with a weighted readout over each token's 24 rows of a layer.
-    fused = None
-    if solo and w.d in (256, 512, 1024) and w.rows_per_token % 24 == 0:
-        group = 24
-        gates = torch.rand(n, dtype=torch.float32, device="cuda",
-                           generator=torch.Generator(device="cuda").manual_seed(5))
-        red_out = torch.empty((n // group, w.d), dtype=torch.bfloat16, device="cuda")
-        tr = time_steps(lambda: cp.lookup_decode_reduce(table, idx, group, gates, red_out, stream),
-                        min(args.steps, 500), args.warmup, flush, stream)
-        tm = float(np.median(tr))
-        fbytes = n * (w.rec_bytes + 8 + 4) + (n // group) * 2 * w.d
-        fused = {"entry_point": "cp_lookup_decode_reduce", "group": group,
-                 "ms_per_step": tm * 1e3, "lookups_per_s": n / tm,
-                 "algorithmic_gbs": fbytes / tm / 1e9, "bytes_per_step": fbytes,
-                 "frac_of_hbm_peak": fbytes / tm / 1e9 / measured_peaks()[0]}
-        inst = ncu_inst("lookup_decode_reduce_kernel", n, w.d, w.k, group)
-        if inst is not None:
-            fused["roofline"] = {"bound": "alu", "achieved": inst / tm,
-                                 "peak": ISSUE_PEAK_WARP_INST_S, "unit": "warp-inst/s",
-                                 "frac": inst / tm / ISSUE_PEAK_WARP_INST_S,
-                                 "peak_kind": "derived: 152 SMs x 4 schedulers x 2.07 GHz",
-                                 "inst_per_launch": inst}
-        del red_out, gates
+    fused = fused_measure(args, w, table, idx, flush, stream) if solo else None
 
     # Mixed per-row bit rates (frequency-based allocation): 2^24 rows x the same d,
     # rates uniform over b = 1.5 .. 3, the same replay shape.
-    mixed = None
-    if w.d % 32 == 0 and w.d <= 4096 and solo:
-        mrows = 1 << 24
-        ks = synth.mixed_rates(synth.SEED_TABLE, torch.arange(mrows, device="cuda"))
-        moffs = synth.mixed_offsets(ks, w.d)
-        mbuf = torch.empty(int(moffs[-1].item()), dtype=torch.uint8, device="cuda")
-        synth.fill_mixed_records(mbuf, synth.SEED_TABLE, ks, moffs, w.d)
-        mtable = cp.load_mixed_table(mbuf, moffs, w.d)
-        midx = torch.from_numpy(synth.zipf_indices(synth.SEED_INDEX, n, mrows)).cuda()
-        mrec = (moffs[1:] - moffs[:-1])[midx].sum().item()
-        tmx = time_steps(lambda: cp.lookup_decode(mtable, midx, out, stream), min(args.steps, 500),
-                         args.warmup, flush, stream)
-        assert cp.get_status(mtable) == cp.CP_OK
-        tmm = float(np.median(tmx))
-        mbytes = mrec + n * (2 * w.d + 8 + 16)
-        mixed = {"entry_point": "cp_lookup_decode (mixed-rate table)", "n_rows": mrows,
-                 "mean_bits_per_param": float(mbuf.numel() * 8 / (mrows * w.d)),
-                 "ms_per_step": tmm * 1e3, "rows_per_s": n / tmm,
-                 "algorithmic_gbs": mbytes / tmm / 1e9,
-                 "frac_of_hbm_peak": mbytes / tmm / 1e9 / measured_peaks()[0]}
-        mtable.close()
-        del mbuf, moffs, ks, midx
+    mixed = mixed_measure(args, w, n, flush, stream) if solo else None
 
     # Offline compression on the GPU (the step before the hot path).
     enc = encoder_measure(args, w) if solo and w.d >= 16 else None
@@ -612,6 +573,65 @@ def our_arm(args, w, rank, world, local):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def fused_measure(args, w, table, idx, flush, stream):
+    """cp_lookup_decode_reduce over each token's 24 rows of a layer, random gates."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    n = idx.numel()
+    if w.d not in (256, 512, 1024) or w.rows_per_token % 24 != 0:
+        return None
+    group = 24
+    gates = torch.rand(n, dtype=torch.float32, device="cuda",
+                       generator=torch.Generator(device="cuda").manual_seed(5))
+    red_out = torch.empty((n // group, w.d), dtype=torch.bfloat16, device="cuda")
+    tr = time_steps(lambda: cp.lookup_decode_reduce(table, idx, group, gates, red_out, stream),
+                    min(args.steps, 500), args.warmup, flush, stream)
+    tm = float(np.median(tr))
+    fbytes = n * (w.rec_bytes + 8 + 4) + (n // group) * 2 * w.d
+    fused = {"entry_point": "cp_lookup_decode_reduce", "group": group,
+             "ms_per_step": tm * 1e3, "lookups_per_s": n / tm,
+             "algorithmic_gbs": fbytes / tm / 1e9, "bytes_per_step": fbytes,
+             "frac_of_hbm_peak": fbytes / tm / 1e9 / measured_peaks()[0]}
+    inst = ncu_inst("lookup_decode_reduce_kernel", n, w.d, w.k, group)
+    if inst is not None:
+        fused["roofline"] = {"bound": "alu", "achieved": inst / tm,
+                             "peak": ISSUE_PEAK_WARP_INST_S, "unit": "warp-inst/s",
+                             "frac": inst / tm / ISSUE_PEAK_WARP_INST_S,
+                             "peak_kind": "derived: 152 SMs x 4 schedulers x 2.07 GHz",
+                             "inst_per_launch": inst}
+    return fused
+
+
+def mixed_measure(args, w, n, flush, stream, mrows: int = 1 << 24):
+    """cp_lookup_decode on a mixed-rate table of mrows rows x the workload's d, rates
+    uniform over b = 1.5 .. 3, a Zipf(1.0) replay of n lookups."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    if w.d % 32 != 0 or w.d > 4096:
+        return None
+    ks = synth.mixed_rates(synth.SEED_TABLE, torch.arange(mrows, device="cuda"))
+    moffs = synth.mixed_offsets(ks, w.d)
+    mbuf = torch.empty(int(moffs[-1].item()), dtype=torch.uint8, device="cuda")
+    synth.fill_mixed_records(mbuf, synth.SEED_TABLE, ks, moffs, w.d)
+    mtable = cp.load_mixed_table(mbuf, moffs, w.d)
+    midx = torch.from_numpy(synth.zipf_indices(synth.SEED_INDEX, n, mrows)).cuda()
+    mout = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    mrec = (moffs[1:] - moffs[:-1])[midx].sum().item()
+    tmx = time_steps(lambda: cp.lookup_decode(mtable, midx, mout, stream), min(args.steps, 500),
+                     args.warmup, flush, stream)
+    assert cp.get_status(mtable) == cp.CP_OK
+    tmm = float(np.median(tmx))
+    mbytes = mrec + n * (2 * w.d + 8 + 16)
+    res = {"entry_point": "cp_lookup_decode (mixed-rate table)", "n_rows": mrows,
+           "mean_bits_per_param": float(mbuf.numel() * 8 / (mrows * w.d)),
+           "ms_per_step": tmm * 1e3, "rows_per_s": n / tmm,
+           "algorithmic_gbs": mbytes / tmm / 1e9,
+           "frac_of_hbm_peak": mbytes / tmm / 1e9 / measured_peaks()[0]}
+    mtable.close()
+    return res
 
 
 def sustained_measure(args, w, table, out, flush, stream, bpl: int):
@@ -788,7 +808,8 @@ def host_path_measure(args, w, idx, flush, stream):
     table = cp.load_table(host, w.n_rows, w.d, w.k, cp.default_lut())
     n = idx.numel()
     out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
-    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), 50, 3, flush, stream)
+    hsteps = min(args.steps, 50) if args.only == "host" else 50
+    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), hsteps, 3, flush, stream)
     assert cp.get_status(table) == cp.CP_OK
     tm = float(np.median(t))
     link_gbs = n * R / tm / 1e9
@@ -798,7 +819,7 @@ def host_path_measure(args, w, idx, flush, stream):
         # frequency-based cache: the 2^20 most frequent rows of the Zipf law in HBM
         hot = synth.feistel_bijection(np.arange(1 << 20), w.n_rows, synth.SEED_INDEX)
         cp.set_cache(table, hot)
-        tc = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), 50, 3, flush,
+        tc = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), hsteps, 3, flush,
                         stream)
         assert cp.get_status(table) == cp.CP_OK
         tcm = float(np.median(tc))
@@ -822,6 +843,36 @@ def host_path_measure(args, w, idx, flush, stream):
                     "id); frac_lookup_bytes counts n * R as the survey's algorithmic bytes"}
 
 
+def only_leg(args, w):
+    """One leg of the bench on its own (the workload's table built only when the leg
+    needs it); steps / warm-up from the command line."""
+    import torch
+    import trellis_row_decode_gb300 as cp
+    from trellis_row_decode_gb300 import synth
+    if args.only == "encoder":
+        return encoder_measure(args, w)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    idx = torch.from_numpy(w.indices(synth.SEED_INDEX)).cuda()
+    n = idx.numel()
+    if args.only == "mixed":
+        return mixed_measure(args, w, n, flush, stream, mrows=args.mixed_rows)
+    if args.only == "host":
+        return host_path_measure(args, w, idx, flush, stream)
+    table, rec, soa = build_table(w, args.layout, synth.SEED_TABLE)
+    if args.only == "reduce":
+        return fused_measure(args, w, table, idx, flush, stream)
+    out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    t = time_steps(lambda: cp.lookup_decode(table, idx, out, stream), args.steps, args.warmup,
+                   flush, stream)
+    assert cp.get_status(table) == cp.CP_OK
+    bpl = w.algorithmic_bytes_per_lookup()
+    tm = float(np.median(t))
+    return {"entry_point": "cp_lookup_decode", "workload": w.name, "layout": args.layout,
+            "ms_per_step": tm * 1e3, "rows_per_s": n / tm, "achieved_gbs": n * bpl / tm / 1e9,
+            "frac_of_hbm_peak": n * bpl / tm / 1e9 / measured_peaks()[0]}
+
+
 def main():
     args = parse()
     from trellis_row_decode_gb300 import synth
@@ -832,11 +883,12 @@ def main():
     if args.impl == "reference":
         reference_arm(args, w, rank)
         return
-    if args.only == "encoder":
+    if args.only is not None:
         import torch
         torch.cuda.set_device(local)
+        res = only_leg(args, w)
         if rank == 0:
-            print(json.dumps({"encoder": encoder_measure(args, w)}), flush=True)
+            print(json.dumps({args.only: res}), flush=True)
         return
     our_arm(args, w, rank, world, local)
 

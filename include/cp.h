@@ -46,7 +46,7 @@
  *   - The caller owns every large buffer (records, SoA copy, ids, output); a
  *     table handle borrows them and they must outlive it.  The handle owns only
  *     its LUT copy, its device status word, its geometry and, for host-resident
- *     tables, 32 MB of device scratch for deduplication and the visiting order.
+ *     tables, 8.4 MB of device scratch for the visiting order.
  *   - Out-of-range ids never fault: the output row is written as zeros and the
  *     table's device status word records CP_ERR_INDEX_OOB for cp_get_status.
  *   - n = 0 is a valid no-op.
@@ -151,7 +151,9 @@ cp_status cp_table_load_mixed(cp_table** out, const void* records, const uint64_
  * Launch (single-rate table): one kernel of ceil(n / 32) CTAs of 256 threads
  * (32 lookups per CTA), each with 8 KB of LUT plus 32 record stages of shared
  * memory (under 18 KB at d = 1024, b = 2); work from other streams can share
- * the SMs.  A mixed-rate table runs one persistent 1024-thread CTA per SM.
+ * the SMs.  A mixed-rate table runs the same grid shape (with stages sized for
+ * the widest rate) and resolves each id to its record's offset and rate inside
+ * the kernel.
  */
 cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                            void* stream);
@@ -162,14 +164,14 @@ cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, ui
  * the host link (zero-copy) [P4 "assumptions and limits"; P1 "Interpretation"].
  * idx and out are device pointers as for cp_lookup_decode; the output is the
  * same, bit for bit, as cp_lookup_decode on the same records.
- * Internally, per pass of at most 2^20 lookups: one lookup per distinct id is
- * elected owner (a device hash table), only owners' records cross the host link,
- * visited grouped by row-id range (a counting partition into 4096 ranges) so
- * that successive host reads are close in the host address space; every other
- * lookup then copies its owner's finished row.  This state lives in 32 MB of
- * device scratch owned by the handle (allocated by cp_table_load), so calls on
- * one host-resident handle must be ordered on one stream (or otherwise
- * serialised).
+ * Internally, per pass of at most 2^20 lookups, the lookups are visited
+ * grouped by row-id range (a counting partition into 4096 ranges), so that
+ * successive host reads are close in the host address space; every row is still
+ * written at its own position.  Repeats of an id fall into the same stretch of
+ * that order and read the record from L2, so about one read per distinct id
+ * crosses the host link.  This state lives in 8.4 MB of device scratch owned by
+ * the handle (allocated by cp_table_load), so calls on one host-resident handle
+ * must be ordered on one stream (or otherwise serialised).
  */
 cp_status cp_lookup_decode_host(const cp_table* t, const int64_t* idx, uint64_t n,
                                 uint16_t* out, void* stream);
@@ -291,12 +293,13 @@ cp_status cp_get_status(const cp_table* t, void* stream);
  *   idx       device, n int64 ids;  out: device bf16 [n][d], 16-byte aligned.
  *   status    device uint32 owned by the caller: bit 0 is OR-ed in when an id is
  *             out of range (clear it yourself before the call if needed).
- * It allocates nothing: its scratch (the LUT copy, the dedupe table, the visiting
- * order) is one static device array of about 2 MB that every GPU loading the
+ * It allocates nothing: its scratch (the LUT copy, the range counts, the visiting
+ * order) is one static device array of about 0.56 MB that every GPU loading the
  * library holds until the process exits.  Limit: n <= 65536 lookups per call;
  * larger n returns CP_ERR_INVALID_ARG before any work is queued.
- * The first call on a device looks up that array's device address (once per
- * device); make that first call before any stream capture.  The address is kept
+ * The first call on a device looks up that array's device address and clears
+ * its counters with a synchronous memset (once per device); make that first call
+ * before any stream capture.  The address is kept
  * for the life of the process: after cudaDeviceReset it no longer names the
  * array, so do not call this entry point on a device that has been reset.  All calls share the
  * array and it keeps the last call's contents (each call clears what must start

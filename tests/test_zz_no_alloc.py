@@ -79,3 +79,25 @@ def test_noalloc_rejects_a_short_records_buffer():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(ValueError):
         cp.lookup_decode_host_noalloc(rec, n_rows, d, k, idx, out, status)
+
+
+def test_noalloc_tables_of_different_sizes_in_turn():
+    """Calls on tables with different numbers of row ranges share the static
+    scratch in turn (its counters must be back at zero after each call)."""
+    d, k = 512, 4
+    lut = cp.default_lut()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tables = {}
+    for n_rows in (300, 50021):
+        tables[n_rows] = synth.gen_records(3, torch.arange(n_rows), d, k).reshape(-1) \
+            .contiguous().pin_memory()
+    for call, (n_rows, seed, n) in enumerate([(50021, 1, 30000), (300, 2, 5000),
+                                              (50021, 3, 65536), (300, 4, 777)]):
+        idx_np = synth.zipf_indices(seed, n, n_rows)
+        idx = torch.from_numpy(idx_np).cuda()
+        out = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+        cp.lookup_decode_host_noalloc(tables[n_rows], n_rows, d, k, idx, out, status)
+        torch.cuda.synchronize()
+        n_bad, ulp = compare(_bits(out).view(np.uint16), oracle_decode(3, d, k, idx_np, n_rows, lut))
+        assert n_bad == 0, f"call {call}: {n_bad} elements differ from the oracle ({ulp} ulp)"
+    assert int(status.item()) == 0

@@ -31,6 +31,8 @@ bool take_injected(std::atomic<int>& c) {
 
 }  // namespace
 
+static_assert(cpk::kBucketBits == cpx::kBucketBitsHost, "one bucket width on both sides");
+
 namespace cpx {
 
 void set_error(const std::string& what) { g_last_error = what; }
@@ -43,33 +45,12 @@ cp_status cuda_fail(cudaError_t e, const char* what) {
 HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb) {
   HostScratch h;
   h.capacity = capacity;
-  h.keys = static_cast<unsigned long long*>(base);
-  h.owner = reinterpret_cast<uint32_t*>(h.keys + 2ull * capacity);
-  h.dup = h.owner + 2ull * capacity;
-  h.counts = h.dup + capacity;
-  h.perm = h.counts + ((nb + 1 + 63) & ~63u);
+  h.counts = static_cast<uint32_t*>(base);
+  h.cursor = h.counts + host_scratch_count_words(nb);
+  h.perm = h.cursor + host_scratch_count_words(nb);
   h.cslot = h.perm + capacity;
   return h;
 }
-
-void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb) {
-  uint32_t bits = 0;
-  while (bits < 64 && ((n_rows - 1) >> bits) != 0) ++bits;
-  *shift = bits > cpk::kBucketBits ? bits - cpk::kBucketBits : 0;
-  *nb = static_cast<uint32_t>(((n_rows - 1) >> *shift) + 1);
-}
-
-bool geometry_ok(uint32_t d, uint32_t k) {
-  if (k < 3 || k > 6) return false;
-  if (d < 8 || d > 4096 || (d % 8) != 0) return false;
-  // whole 16-bit words per record, so every record starts 2-byte aligned
-  if ((static_cast<uint64_t>(d) * k) % 32 != 0) return false;
-  return true;
-}
-
-uint32_t soa_stride(uint32_t d, uint32_t k) { return ((d * k / 16) + 15u) & ~15u; }
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 cpk::KernelSet kernels_for(uint32_t k) {
   switch (k) {
@@ -80,19 +61,8 @@ cpk::KernelSet kernels_for(uint32_t k) {
   }
 }
 
-// Stage size in bytes for a geometry: a 16-byte prefix (room for the spliced
-// code tail below bit 0), the 16-byte aligned span that holds the record
-// (misalignment <= 14 bytes for AoS), and 16 bytes of slack for the 64-bit
-// funnel reads past the code; SoA adds the 4-byte alpha slot in that slack.
 uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot) {
-  const uint32_t pre = cpk::kStagePrefix;
-  if (soa) {
-    *alpha_slot = pre + t->soa_stride + 8;
-    return pre + t->soa_stride + 16;
-  }
-  *alpha_slot = 0;
-  const uint32_t span = t->code_bytes + 2 + 14;
-  return pre + ((span + 15u) & ~15u) + 16u;
+  return stage_bytes_for(cpk::kStagePrefix, t->code_bytes, t->soa_stride, soa, alpha_slot);
 }
 
 cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
@@ -168,32 +138,20 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     g_last_error = "too many lookups for one launch";
     return CP_ERR_INVALID_ARG;
   }
-  // Per pass of at most hs->capacity lookups: elect one owner per distinct id,
-  // partition the owners by row range, decode them in that order (each row
-  // lands at its own position), then fill the other lookups from their owner's
-  // row.
-  unsigned long long* keys = hs->keys;
-  uint32_t* owner = hs->owner;
-  uint32_t* dup = hs->dup;
-  uint32_t* counts = hs->counts;
-  uint32_t* perm = hs->perm;
+  // Per pass of at most hs->capacity lookups: partition the lookups by row
+  // range, then decode them in that order (each row lands at its own position;
+  // repeats of an id read its record from L2).
   const uint64_t cap = hs->capacity;
+  const bool cached = t->cache != nullptr && t->cmap_ts != 0;
   for (uint64_t c0 = 0; c0 < n; c0 += cap) {
     const uint64_t m = (n - c0 < cap) ? n - c0 : cap;
-    uint32_t ts = 1024;
-    while (ts < 2 * m) ts <<= 1;
-    const bool cached = t->cache != nullptr && t->cmap_ts != 0;
-    cpk::launch_dedupe(idx + c0, m, t->n_rows, keys, owner, ts, dup,
-                       cached ? t->cmap_keys : nullptr, cached ? t->cmap_vals : nullptr,
-                       cached ? t->cmap_ts : 0,
-                       cached ? hs->cslot : nullptr, t->bucket_shift, t->bucket_nb, counts,
-                       t->sm_count, stream);
-    cpk::launch_bucket_partition(idx + c0, dup, m, t->n_rows, t->bucket_shift, t->bucket_nb,
-                                 counts, perm, t->sm_count, stream);
+    cpk::launch_bucket_partition(idx + c0, m, t->n_rows, cached ? t->cmap_keys : nullptr,
+                                 cached ? t->cmap_vals : nullptr, cached ? t->cmap_ts : 0,
+                                 hs->cslot, t->bucket_shift, t->bucket_nb, hs->counts,
+                                 hs->cursor, hs->perm, t->sm_count, stream);
     cpk::DecodeParams pc = p;
     pc.idx = idx + c0;
-    pc.perm = perm;
-    pc.n_dev = counts + t->bucket_nb;                   // visits = owners + out-of-range ids
+    pc.perm = hs->perm;
     if (cached) {
       pc.cslot = hs->cslot;
       pc.cache = t->cache;
@@ -207,7 +165,6 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
     e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(bl)),
                          dim3(nwarps * 32), args, smem, stream);
     if (e != cudaSuccess) return cuda_fail(e, "host lookup-decode launch");
-    cpk::launch_copy_dups(dup, m, t->d, out + c0 * t->d, t->sm_count, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "host path launch");
   }
@@ -226,7 +183,7 @@ using cpx::kMaxLookups;
 using cpx::kMaxRows;
 using cpx::soa_stride;
 
-// Mixed-rate table: a persistent decode kernel with the rate chosen per row.
+// Mixed-rate table: the non-persistent block kernel with the rate taken per row.
 cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16_t* out,
                        cudaStream_t stream) {
   cpk::DecodeParams p;
@@ -243,27 +200,28 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
   p.n = n;
   p.out = out;
   p.status = t->status_dev;
-  const int pf = cpk::kPfMixed;
-  int nwarps = cpk::kMaxWarps;
-  auto smem_for = [&](int w) {
-    return static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepMixed)) +
-           static_cast<size_t>(w) * pf * (p.stage_bytes + 8);
-  };
-  while (nwarps > 1 && smem_for(nwarps) > static_cast<size_t>(t->max_smem)) nwarps >>= 1;
-  const size_t smem = smem_for(nwarps);
-  if (smem > static_cast<size_t>(t->max_smem)) return CP_ERR_INVALID_ARG;
+  const int rows = cpk::mixed_rows_per_warp();
+  const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepBlock)) +
+                      static_cast<size_t>(cpk::kBlkWarps) * rows * p.stage_bytes;
+  if (smem > static_cast<size_t>(t->max_smem)) {
+    g_last_error = "geometry needs more shared memory than the device offers";
+    return CP_ERR_INVALID_ARG;
+  }
+  const uint64_t per_block = static_cast<uint64_t>(cpk::kBlkWarps) * rows;
+  const uint64_t blocks = (n + per_block - 1) / per_block;
+  if (blocks > 0x7FFFFFFFull) {
+    g_last_error = "too many lookups for one launch";
+    return CP_ERR_INVALID_ARG;
+  }
   cpk::MixedFn fn = cpk::mixed_kernel(cpk::cpl_index(t->d));
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  uint64_t blocks = (n + nwarps - 1) / nwarps;
-  if (blocks > static_cast<uint64_t>(t->sm_count)) blocks = t->sm_count;
-  if (n / (blocks * nwarps) >= (1ull << 31)) return CP_ERR_INVALID_ARG;
   const uint64_t* offsets = t->offsets;
   void* args[] = {&p, &offsets};
   e = cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(static_cast<unsigned>(blocks)),
-                       dim3(nwarps * 32), args, smem, stream);
+                       dim3(cpk::kBlkWarps * 32), args, smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "mixed lookup-decode launch");
   return CP_OK;
 }
@@ -442,6 +400,14 @@ cp_status cp_table_load(cp_table** out, const void* records, uint64_t n_rows, ui
       cuda_fail(e, "cudaMalloc(bucket scratch)");
       cp_table_free(t);
       return CP_ERR_NO_MEMORY;
+    }
+    // range counts start at zero; every pass leaves them at zero again
+    e = cudaMemsetAsync(t->scratch_dev, 0,
+                        cpx::host_scratch_count_words(t->bucket_nb) * sizeof(uint32_t), s);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "scratch clear");
+      cp_table_free(t);
+      return st;
     }
     void* dptr = nullptr;
     if (take_injected(g_fail_register)) {

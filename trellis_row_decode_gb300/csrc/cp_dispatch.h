@@ -23,9 +23,11 @@ using DecodeFn = void (*)(DecodeParams);
 using ReduceFn = void (*)(DecodeParams, const float*, uint32_t, uint64_t);
 using MixedFn = void (*)(DecodeParams, const uint64_t*);
 
-// Mixed-rate tables (one bit rate per row): kernel for a chunks-per-lane index
-// and the load-time check of the offset table (bad = 1 when a record is unusable).
+// Mixed-rate tables (one bit rate per row): the block kernel for a
+// chunks-per-lane index (kBlkWarps * mixed_rows_per_warp() lookups per CTA) and
+// the load-time check of the offset table (bad = 1 when a record is unusable).
 MixedFn mixed_kernel(int cpl_idx);
+int mixed_rows_per_warp();
 void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
                         int sm_count, cudaStream_t s);
 
@@ -70,23 +72,8 @@ constexpr int kPfHostReg = 8;
 
 // Host-resident tables: lookups are visited bucketed by row-id range so that
 // consecutive records of a warp are close in the host address space.
-constexpr uint32_t kBucketBits = 12;                  // 4096 ranges
+constexpr uint32_t kBucketBits = 12;                  // 4096 ranges (cpx::kBucketBitsHost)
 constexpr uint32_t kBucketChunk = 1u << 20;           // lookups per pass
-constexpr uint32_t kHashSlotsMax = 2 * kBucketChunk;  // dedupe table slots (load <= 1/2)
-
-// dup[j] = owner lookup of idx[j] among n lookups (kNoOwner for ids outside
-// [0, n_rows)); keys (ts 64-bit words) and owner (ts words) are the
-// open-addressing table, ts a power of two >= 2n, emptied by a reset kernel that
-// this call queues first.
-// With a hot-row cache map (cmap_ts > 0), also cslot[j] = cache slot of idx[j]
-// (or 0xFFFFFFFF when the id is not cached).
-// counts (nb + 1 words, zeroed by the same reset) receives the number of lookups
-// to visit per bucket (id >> shift): the owners, and in bucket nb the ids out of range.
-void launch_dedupe(const int64_t* idx, uint64_t n, uint64_t n_rows, unsigned long long* keys,
-                   uint32_t* owner, uint32_t ts, uint32_t* dup,
-                   const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
-                   uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,
-                   uint32_t* counts, int sm_count, cudaStream_t s);
 
 // Hot-row cache construction: records of the m rows `rows` (device ids, sorted)
 // copied from the host table alias into `cache` (stride R), and the map
@@ -95,16 +82,17 @@ void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, u
                         uint8_t* cache, unsigned long long* keys, uint32_t* vals, uint32_t ts,
                         int sm_count, cudaStream_t s);
 
-// Partition of the lookups that own their id by (id >> shift), ids outside
-// [0, n_rows) in the last bucket.  counts: the nb + 1 per-bucket visit counts
-// from launch_dedupe; afterwards counts[nb] = number of visits.
-void launch_bucket_partition(const int64_t* idx, const uint32_t* dup, uint64_t n, uint64_t n_rows,
-                             uint32_t shift, uint32_t nb, uint32_t* counts, uint32_t* perm,
-                             int sm_count, cudaStream_t s);
-
-// out row j = out row dup[j] for every non-owner lookup j.
-void launch_copy_dups(const uint32_t* dup, uint64_t n, uint32_t d, uint16_t* out, int sm_count,
-                      cudaStream_t s);
+// Visiting order of n lookups for a host-resident table: perm = the lookups
+// grouped by range (id >> shift; range nb: ids outside [0, n_rows)), a counting
+// partition (count, scan, scatter).  With a cache map (cmap_ts > 0) cslot[j]
+// receives the cache slot of idx[j] or 0xFFFFFFFF.  counts (nb + 1 words) must
+// hold zeros on entry and holds zeros again afterwards; cursor (nb + 1 words)
+// is scratch.
+void launch_bucket_partition(const int64_t* idx, uint64_t n, uint64_t n_rows,
+                             const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
+                             uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,
+                             uint32_t* counts, uint32_t* cursor, uint32_t* perm, int sm_count,
+                             cudaStream_t s);
 
 KernelSet kernels_k3();
 KernelSet kernels_k4();

@@ -8,6 +8,7 @@
 
 #include "cp.h"
 #include "cp_dispatch.h"
+#include "cp_geometry.h"
 
 struct cp_table {
   int device;
@@ -42,36 +43,20 @@ struct cp_table {
 
 namespace cpx {
 
-constexpr uint64_t kMaxRows = 1ull << 40;
-constexpr uint64_t kMaxLookups = 1ull << 40;
-
 // Device scratch of the host-resident path for passes of up to `capacity`
-// lookups: the dedupe table (2 * capacity slots of 64-bit keys and 32-bit
-// owners), the owner of each lookup, the bucket counts and the visiting order.
+// lookups: per-range counts (zero between passes) and cursors, the visiting
+// order and the cache slot of each lookup.
 struct HostScratch {
-  unsigned long long* keys;
-  uint32_t* owner;
-  uint32_t* dup;
-  uint32_t* counts;
-  uint32_t* perm;
-  uint32_t* cslot;        // cache slot of each lookup's id (hot-row cache), else ~0
+  uint32_t* counts;       // nb + 1 words, zero on entry and exit of a pass
+  uint32_t* cursor;       // nb + 1 words
+  uint32_t* perm;         // capacity words
+  uint32_t* cslot;        // capacity words: cache slot of each lookup's id (hot-row cache)
   uint32_t capacity;
 };
 
-constexpr size_t host_scratch_bytes(uint32_t capacity, uint32_t nb) {
-  return static_cast<size_t>(2) * capacity * (sizeof(unsigned long long) + sizeof(uint32_t)) +
-         (static_cast<size_t>(3) * capacity + ((nb + 1 + 63) & ~63u)) * sizeof(uint32_t);
-}
-
 HostScratch host_scratch_layout(void* base, uint32_t capacity, uint32_t nb);
 
-// Bucket shift and count for n_rows rows: at most 2^kBucketBits ranges.
-void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb);
-
-bool geometry_ok(uint32_t d, uint32_t k);
 uint32_t stage_bytes(const cp_table* t, bool soa, uint32_t* alpha_slot);
-uint32_t soa_stride(uint32_t d, uint32_t k);
-bool aligned(const void* p, uintptr_t a);
 cpk::KernelSet kernels_for(uint32_t k);
 void set_error(const std::string& what);
 cp_status cuda_fail(cudaError_t e, const char* what);

@@ -79,7 +79,6 @@ struct DecodeParams {
   const uint32_t* lut;      // 512 words: fp16 y0 (low half) | fp16 y1 (high half)
   const int64_t* idx;
   const uint32_t* perm;     // processing order (PERM kernels): position i decodes lookup perm[i]
-  const uint32_t* n_dev;    // PERM kernels: number of positions, read on the device
   const uint32_t* cslot;    // host path: cache slot per lookup (0xFFFFFFFF: not cached) or null
   const uint8_t* cache;     // host path: device copies of hot records, stride = record bytes
   uint64_t cache_bytes;
@@ -396,11 +395,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) lookup_decode_kernel(const 
 
   const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
-  uint64_t n_work = p.n;
-  if (PERM && p.n_dev != nullptr) {
-    const uint64_t nd = *p.n_dev;                        // <= p.n by construction
-    n_work = nd < p.n ? nd : p.n;
-  }
+  const uint64_t n_work = p.n;
   const uint64_t lo = gw * n_work / W;
   const uint64_t hi = (gw + 1) * n_work / W;
   if (lo >= hi) return;

@@ -24,16 +24,25 @@ __global__ void check_mixed_offsets_kernel(const uint64_t* __restrict__ offsets,
   }
 }
 
+namespace {
+#ifndef CP_MIXED_ROWS
+#define CP_MIXED_ROWS 4
+#endif
+constexpr int kMixedRows = CP_MIXED_ROWS;                // rows per warp (a multiple of 4)
+}
+
 MixedFn mixed_kernel(int cpl_idx) {
   switch (cpl_idx) {
-    case 1: return &lookup_decode_mixed_kernel<1>;
-    case 2: return &lookup_decode_mixed_kernel<2>;
-    case 3: return &lookup_decode_mixed_kernel<4>;
-    case 4: return &lookup_decode_mixed_kernel<8>;
-    case 5: return &lookup_decode_mixed_kernel<16>;
-    default: return &lookup_decode_mixed_kernel<0>;
+    case 1: return &lookup_decode_mixed_block_kernel<1, kLutRepBlock, kMixedRows>;
+    case 2: return &lookup_decode_mixed_block_kernel<2, kLutRepBlock, kMixedRows>;
+    case 3: return &lookup_decode_mixed_block_kernel<4, kLutRepBlock, kMixedRows>;
+    case 4: return &lookup_decode_mixed_block_kernel<8, kLutRepBlock, kMixedRows>;
+    case 5: return &lookup_decode_mixed_block_kernel<16, kLutRepBlock, kMixedRows>;
+    default: return &lookup_decode_mixed_block_kernel<0, kLutRepBlock, kMixedRows>;
   }
 }
+
+int mixed_rows_per_warp() { return kMixedRows; }
 
 void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
                         int sm_count, cudaStream_t s) {

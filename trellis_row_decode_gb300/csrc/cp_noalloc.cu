@@ -8,8 +8,8 @@
 // (LUT copy, status word, 32 MB of scratch for host-resident tables), so those
 // callers use cp_lookup_decode_host_noalloc instead: it takes the records, the
 // LUT, the ids, the output and a status word from the caller, and keeps its own
-// scratch (LUT copy, dedupe table, visiting order) in one file-scope device
-// array, sized for at most kNoAllocMaxLookups lookups per call.
+// scratch (LUT copy, range counts and cursors, visiting order) in one
+// file-scope device array, sized for at most kNoAllocMaxLookups lookups per call.
 #include <cstdint>
 #include <mutex>
 
@@ -26,7 +26,7 @@ constexpr size_t kLutDevBytes = 512 * sizeof(uint32_t);
 constexpr size_t kNoAllocScratchBytes =
     kLutDevBytes + cpx::host_scratch_bytes(kNoAllocMaxLookups, kNoAllocMaxBuckets);
 
-// About 2 MB on every GPU that loads the library, held until the process exits.
+// About 0.5 MB on every GPU that loads the library, held until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -34,7 +34,8 @@ std::mutex g_setup_mu;
 unsigned char* g_scratch_addr[kMaxDevices];   // device address of the array, per device
 
 // Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the host-side name of the array is not a device address).
+// per device (the host-side name of the array is not a device address).  The
+// same set-up clears the range counts, which every call then leaves at zero.
 cp_status scratch_for_device(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) {
     cpx::set_error("device ordinal outside the supported range");
@@ -43,8 +44,12 @@ cp_status scratch_for_device(int dev, unsigned char** out) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cpx::cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    e = cudaMemset(static_cast<unsigned char*>(p) + kLutDevBytes, 0,
+                   cpx::host_scratch_count_words(kNoAllocMaxBuckets) * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cpx::cuda_fail(e, "no-alloc scratch clear");
     g_scratch_addr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_scratch_addr[dev];
@@ -116,7 +121,9 @@ extern "C" cp_status cp_lookup_decode_host_noalloc(const void* records, uint64_t
   t.kernels = cpx::kernels_for(bits_per_step);
   cudaDeviceGetAttribute(&t.sm_count, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&t.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  // laid out for the largest bucket count, so that the counts (zero between
+  // calls) never overlap the cursors of a call on a table with fewer ranges
   const cpx::HostScratch hs =
-      cpx::host_scratch_layout(t.scratch_dev, kNoAllocMaxLookups, t.bucket_nb);
+      cpx::host_scratch_layout(t.scratch_dev, kNoAllocMaxLookups, kNoAllocMaxBuckets);
   return cpx::launch_decode(&t, idx, n, out, s, true, &hs);
 }

@@ -200,7 +200,8 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
   p.n = n;
   p.out = out;
   p.status = t->status_dev;
-  const int rows = cpk::mixed_rows_per_warp();
+  const int ci = cpk::cpl_index(t->d);
+  const int rows = cpk::mixed_rows_per_warp(ci);
   const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepBlock)) +
                       static_cast<size_t>(cpk::kBlkWarps) * rows * p.stage_bytes;
   if (smem > static_cast<size_t>(t->max_smem)) {
@@ -213,7 +214,7 @@ cp_status launch_mixed(const cp_table* t, const int64_t* idx, uint64_t n, uint16
     g_last_error = "too many lookups for one launch";
     return CP_ERR_INVALID_ARG;
   }
-  cpk::MixedFn fn = cpk::mixed_kernel(cpk::cpl_index(t->d));
+  cpk::MixedFn fn = cpk::mixed_kernel(ci);
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

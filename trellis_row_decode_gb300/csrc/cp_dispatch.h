@@ -24,10 +24,11 @@ using ReduceFn = void (*)(DecodeParams, const float*, uint32_t, uint64_t);
 using MixedFn = void (*)(DecodeParams, const uint64_t*);
 
 // Mixed-rate tables (one bit rate per row): the block kernel for a
-// chunks-per-lane index (kBlkWarps * mixed_rows_per_warp() lookups per CTA) and
-// the load-time check of the offset table (bad = 1 when a record is unusable).
+// chunks-per-lane index (kBlkWarps * mixed_rows_per_warp(cpl_idx) lookups per
+// CTA) and the load-time check of the offset table (bad = 1 when a record is
+// unusable).
 MixedFn mixed_kernel(int cpl_idx);
-int mixed_rows_per_warp();
+int mixed_rows_per_warp(int cpl_idx);
 void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
                         int sm_count, cudaStream_t s);
 

@@ -13,9 +13,11 @@
 //     the output in a narrow window and SMs that reach memory faster (the
 //     imbalance between SMs is systematic on this part) take more CTAs.  With
 //     ~40 rows per warp in static ranges, a persistent grid ran 10-20 % longer;
-//   * host-resident tables (bucketed order): one persistent CTA per SM, each
-//     warp a contiguous range of positions and a ring of PF record stages, PF-1
-//     rows ahead of the row being decoded;
+//   * host-resident tables (lookups visited grouped by row range): one
+//     persistent CTA per SM over a contiguous slice of that order, a ring of PF
+//     records per warp, PF-1 rows ahead of the row being decoded (the register
+//     ring kernel of cp_kernels_host.cuh hands its slice to its warps in chunks
+//     of 32; the kernel here, for d > 1024, gives each warp a fixed range);
 //   * the record of a row is copied with 16-byte cp.async (L2 only) into a
 //     shared-memory stage; the block kernel queues all of a warp's rows before
 //     the CTA builds its LUT, so record latency overlaps the fill; the last

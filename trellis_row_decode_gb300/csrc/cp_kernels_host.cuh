@@ -27,13 +27,15 @@ __device__ __forceinline__ uint4 load_partial16(const uint8_t* src, uint32_t byt
                     static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
 }
 
-// Work distribution: each warp takes a contiguous range of the visiting order
-// (lookups grouped by row range), so each SM reads from one contiguous slice of
-// the table.  Handing out small chunks in order from a global counter balanced
-// the SMs but let every SM's reads span the whole table, and on a 51 GB table
-// that ran 14 times slower (the device's address translation for host memory
-// lost its locality).
-template <int K, bool SOA, int PF, int CPL, int REP, bool PERM = true>
+// Work distribution: each CTA (one per SM) takes a contiguous slice of the
+// visiting order (lookups grouped by row range), so each SM reads from one
+// contiguous part of the table, and its warps take chunks of 32 visits of the
+// slice from a shared-memory counter, so they finish together.  Handing out
+// chunks of the whole order from one global counter balanced the SMs too, but
+// let every SM's reads span the whole table, and on a 51 GB table that ran 14
+// times slower (the device's address translation for host memory lost its
+// locality); fixed ranges per warp left SMs idle 13 % of the time.
+template <int K, bool SOA, int PF, int CPL, int REP>
 __global__ void __launch_bounds__(kHostWarps * 32, 1)
     lookup_decode_host_kernel(const DecodeParams p) {
   static_assert(CPL >= 1 && CPL <= 4, "one 16-byte piece per lane");
@@ -60,42 +62,40 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
   const uintptr_t tbl_end = codes + p.table_bytes;
   uint8_t* sb = smem + kLutBytes + static_cast<size_t>(warp) * p.stage_bytes + kStagePrefix;
 
-  const uint64_t W = static_cast<uint64_t>(gridDim.x) * nwarps;
-  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * nwarps + warp;
+  // each CTA a contiguous slice of the visiting order; its warps take chunks of
+  // 32 visits of the slice from a shared-memory counter (a chunk of look-ahead)
+  __shared__ uint32_t s_ctr;
+  if (tid == 0) s_ctr = 0;
+  __syncthreads();
   const uint64_t n_work = p.n;
-  const uint64_t lo = gw * n_work / W;
-  const uint64_t hi = (gw + 1) * n_work / W;
-  if (lo >= hi) return;
-  const uint32_t cnt = static_cast<uint32_t>(hi - lo);
-
-  // visiting order: positions j = perm[lo + q] (or lo + q), their ids and, with a
-  // hot-row cache, their cache slots, 32 at a time
-  const uint32_t* pos = PERM ? p.perm + lo : nullptr;
-  const uint32_t* cslot = PERM ? p.cslot : nullptr;
+  const uint64_t c_lo = static_cast<uint64_t>(blockIdx.x) * n_work / gridDim.x;
+  const uint64_t c_hi = static_cast<uint64_t>(blockIdx.x + 1) * n_work / gridDim.x;
+  constexpr uint32_t kPast = 0xFFFFFFFFu;
+  const uint32_t* cslot = p.cslot;
   const uintptr_t cache = reinterpret_cast<uintptr_t>(p.cache);
   const uintptr_t cache_end = cache + p.cache_bytes;
-  auto load_batch = [&](uint32_t q, uint32_t& j, int64_t& r, uint32_t& c) {
-    j = 0;
+  auto grab = [&]() -> uint64_t {
+    uint32_t c = 0;
+    if (lane == 0) c = atomicAdd(&s_ctr, 32u);
+    return c_lo + __shfl_sync(0xffffffffu, c, 0);
+  };
+  auto load_batch = [&](uint64_t c, uint32_t& j, int64_t& r, uint32_t& cs) {
+    j = kPast;
     r = 0;
-    c = 0xFFFFFFFFu;
-    if (q < cnt) {
-      if (PERM) {
-        j = __ldg(pos + q);
-        r = __ldg(p.idx + j);
-        if (cslot != nullptr) c = __ldg(cslot + j);
-      } else {
-        j = static_cast<uint32_t>(q);
-        r = __ldg(p.idx + lo + q);
-      }
+    cs = 0xFFFFFFFFu;
+    const uint64_t q = c + lane;
+    if (q < c_hi) {
+      j = __ldg(p.perm + q);
+      r = __ldg(p.idx + j);
+      if (cslot != nullptr) cs = __ldg(cslot + j);
     }
   };
   uint32_t jb_cur, jb_nxt, cb_cur, cb_nxt;
   int64_t ib_cur, ib_nxt;
-  load_batch(lane, jb_cur, ib_cur, cb_cur);
-  load_batch(lane + 32, jb_nxt, ib_nxt, cb_nxt);
+  load_batch(grab(), jb_cur, ib_cur, cb_cur);
+  load_batch(grab(), jb_nxt, ib_nxt, cb_nxt);
   uint32_t batch = 0;
 
-  // ring slot of a row: its 16-byte piece, flags | mis << 8, output row, alpha (SoA)
   uint4 rv[PF];
   uint32_t rm[PF], rj[PF];
   uint16_t ra[PF];
@@ -106,14 +106,14 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
       ib_cur = ib_nxt;
       jb_cur = jb_nxt;
       cb_cur = cb_nxt;
-      load_batch(batch + 32 + lane, jb_nxt, ib_nxt, cb_nxt);
+      load_batch(grab(), jb_nxt, ib_nxt, cb_nxt);
     }
     const int64_t r = __shfl_sync(0xffffffffu, ib_cur, static_cast<int>(q - batch));
     jrow = __shfl_sync(0xffffffffu, jb_cur, static_cast<int>(q - batch));
     const uint32_t cs = __shfl_sync(0xffffffffu, cb_cur, static_cast<int>(q - batch));
     m = 0;
+    if (jrow == kPast) return;
     if (static_cast<uint64_t>(r) < n_rows) {
-      // a cached id reads its AoS record from HBM (cache slots are AoS, stride R)
       const bool hot = !SOA && cs != 0xFFFFFFFFu;
       const uintptr_t a = hot ? cache + static_cast<uint64_t>(cs) * stride
                               : codes + static_cast<uint64_t>(r) * stride;
@@ -135,20 +135,20 @@ __global__ void __launch_bounds__(kHostWarps * 32, 1)
   };
 
 #pragma unroll
-  for (int s = 0; s < PF - 1; ++s)
-    if (static_cast<uint32_t>(s) < cnt) issue(s, rv[s], rm[s], rj[s], ra[s]);
+  for (int s = 0; s < PF - 1; ++s) issue(s, rv[s], rm[s], rj[s], ra[s]);
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (uint32_t g = 0; g < cnt; g += PF) {
+  bool done = false;
+  for (uint32_t g = 0; !done; g += PF) {
 #pragma unroll
     for (int s = 0; s < PF; ++s) {
-      const uint32_t i = g + s;
-      if (i < cnt) {
-        const int sn = (s + PF - 1) % PF;                // slot of row i + PF - 1
-        if (i + PF - 1 < cnt) issue(i + PF - 1, rv[sn], rm[sn], rj[sn], ra[sn]);
+      if (!done && rj[s] == kPast) done = true;
+      if (!done) {
+        const uint32_t i = g + s;
+        const int sn = (s + PF - 1) % PF;
+        issue(i + PF - 1, rv[sn], rm[sn], rj[sn], ra[sn]);
         const uint32_t m = rm[s];
-        uint4* orow = reinterpret_cast<uint4*>(p.out) +
-                      (PERM ? static_cast<uint64_t>(rj[s]) : lo + i) * (d >> 3);
+        uint4* orow = reinterpret_cast<uint4*>(p.out) + static_cast<uint64_t>(rj[s]) * (d >> 3);
         if (m & 1u) {
           const uint32_t mis = m >> 8;
           const uint32_t nch = (mis + code_bytes + (SOA ? 0u : 2u) + 15) >> 4;

@@ -25,16 +25,17 @@ __global__ void check_mixed_offsets_kernel(const uint64_t* __restrict__ offsets,
 }
 
 namespace {
-#ifndef CP_MIXED_ROWS
-#define CP_MIXED_ROWS 4
-#endif
-constexpr int kMixedRows = CP_MIXED_ROWS;                // rows per warp (a multiple of 4)
+// Rows per warp: 8 where a warp decodes several short rows per step (d = 256,
+// 512: 0.047 -> 0.045 ms on the 2^24-row d = 512 table), 4 elsewhere (8 took
+// d = 1024 from 0.078 to 0.086 ms).
+constexpr int kMixedRowsShort = 8;
+constexpr int kMixedRows = 4;
 }
 
 MixedFn mixed_kernel(int cpl_idx) {
   switch (cpl_idx) {
-    case 1: return &lookup_decode_mixed_block_kernel<1, kLutRepBlock, kMixedRows>;
-    case 2: return &lookup_decode_mixed_block_kernel<2, kLutRepBlock, kMixedRows>;
+    case 1: return &lookup_decode_mixed_block_kernel<1, kLutRepBlock, kMixedRowsShort>;
+    case 2: return &lookup_decode_mixed_block_kernel<2, kLutRepBlock, kMixedRowsShort>;
     case 3: return &lookup_decode_mixed_block_kernel<4, kLutRepBlock, kMixedRows>;
     case 4: return &lookup_decode_mixed_block_kernel<8, kLutRepBlock, kMixedRows>;
     case 5: return &lookup_decode_mixed_block_kernel<16, kLutRepBlock, kMixedRows>;
@@ -42,7 +43,9 @@ MixedFn mixed_kernel(int cpl_idx) {
   }
 }
 
-int mixed_rows_per_warp() { return kMixedRows; }
+int mixed_rows_per_warp(int cpl_idx) {
+  return (cpl_idx == 1 || cpl_idx == 2) ? kMixedRowsShort : kMixedRows;
+}
 
 void launch_check_mixed(const uint64_t* offsets, uint64_t n_rows, uint32_t d, uint32_t* bad,
                         int sm_count, cudaStream_t s) {

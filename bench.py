@@ -388,8 +388,10 @@ def torch_int64():
     return torch.int64
 
 
-def time_steps(fn, steps, warmup, flush, stream):
-    """Per-step device times (s) of fn() with an L2 flush between steps."""
+def time_steps(fn, steps, warmup, flush, stream, nvtx: str = "timed"):
+    """Per-step device times (s) of fn() with an L2 flush between steps.  Each timed
+    call is wrapped in an NVTX range `nvtx`, so a profiler filtered on "timed" sees
+    exactly the launches the CUDA events time (not the flushes)."""
     import torch
     for _ in range(warmup):
         fn()
@@ -397,14 +399,14 @@ def time_steps(fn, steps, warmup, flush, stream):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
-    torch.cuda.nvtx.range_push("timed")
     for a, b in ev:
         a.record(stream)
+        torch.cuda.nvtx.range_push(nvtx)
         fn()
+        torch.cuda.nvtx.range_pop()
         b.record(stream)
         flush_l2(flush)
     torch.cuda.synchronize()
-    torch.cuda.nvtx.range_pop()
     return np.array([a.elapsed_time(b) * 1e-3 for a, b in ev])
 
 
@@ -414,7 +416,7 @@ def hbm_same_run(flush, stream, steps: int = 20):
     import torch
     src = torch.ones(1 << 30, dtype=torch.uint8, device="cuda")
     dst = torch.empty_like(src)
-    tc = time_steps(lambda: dst.copy_(src), steps, 3, flush, stream)
+    tc = time_steps(lambda: dst.copy_(src), steps, 3, flush, stream, "copy")
     del src, dst
     return {"copy_gbs": 2 * (1 << 30) / float(np.median(tc)) / 1e9,
             "copy": "torch copy_ of a 1 GiB device buffer, read + write bytes, median of "
@@ -459,7 +461,7 @@ def our_arm(args, w, rank, world, local):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        t = time_steps(step, args.steps, args.warmup, flush, stream)
+        t = time_steps(step, args.steps, args.warmup, flush, stream, "step")
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -505,7 +507,7 @@ def our_arm(args, w, rank, world, local):
         idx_d.copy_(idx_h, non_blocking=True)
         cp.lookup_decode(table, idx_d, out_h, stream)
 
-    te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream)
+    te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream, "e2e")
     _, e2e_value = aggregate(float(te.sum()), n * args.e2e_steps, world, dist, "cuda")
 
     host_obj = None
@@ -587,7 +589,7 @@ def fused_measure(args, w, table, idx, flush, stream):
                        generator=torch.Generator(device="cuda").manual_seed(5))
     red_out = torch.empty((n // group, w.d), dtype=torch.bfloat16, device="cuda")
     tr = time_steps(lambda: cp.lookup_decode_reduce(table, idx, group, gates, red_out, stream),
-                    min(args.steps, 500), args.warmup, flush, stream)
+                    min(args.steps, 500), args.warmup, flush, stream, "reduce")
     tm = float(np.median(tr))
     fbytes = n * (w.rec_bytes + 8 + 4) + (n // group) * 2 * w.d
     fused = {"entry_point": "cp_lookup_decode_reduce", "group": group,
@@ -621,7 +623,7 @@ def mixed_measure(args, w, n, flush, stream, mrows: int = 1 << 24):
     mout = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
     mrec = (moffs[1:] - moffs[:-1])[midx].sum().item()
     tmx = time_steps(lambda: cp.lookup_decode(mtable, midx, mout, stream), min(args.steps, 500),
-                     args.warmup, flush, stream)
+                     args.warmup, flush, stream, "mixed")
     assert cp.get_status(mtable) == cp.CP_OK
     tmm = float(np.median(tmx))
     mbytes = mrec + n * (2 * w.d + 8 + 16)
@@ -736,7 +738,7 @@ def other_configs(args, w, table, idx, out, flush, stream):
         oidx = torch.from_numpy(ow.indices()).cuda()
         oout = torch.empty((oidx.numel(), ow.d), dtype=torch.bfloat16, device="cuda")
         t = time_steps(lambda: cp.lookup_decode(tab, oidx, oout, stream), steps, args.warmup,
-                       flush, stream)
+                       flush, stream, "configs")
         assert cp.get_status(tab) == cp.CP_OK
         res[name] = entry(ow, oidx.numel(), float(np.median(t)))
         if not same_table:
@@ -751,7 +753,7 @@ def other_configs(args, w, table, idx, out, flush, stream):
         oidx = torch.from_numpy(ow.indices()).cuda()
         oout = torch.empty((oidx.numel(), ow.d), dtype=torch.bfloat16, device="cuda")
         t = time_steps(lambda: cp.lookup_decode(tab, oidx, oout, stream), steps, args.warmup,
-                       flush, stream)
+                       flush, stream, "configs")
         assert cp.get_status(tab) == cp.CP_OK
         res["sweep_b2 (SoA layout)"] = entry(ow, oidx.numel(), float(np.median(t)))
         tab.close()
@@ -768,7 +770,7 @@ def other_configs(args, w, table, idx, out, flush, stream):
         def two():
             cp.lookup_decode(table, parts[0], outs[0], stream)
             cp.lookup_decode(table, parts[1], outs[1], stream)
-        t = time_steps(two, steps, args.warmup, flush, stream)
+        t = time_steps(two, steps, args.warmup, flush, stream, "configs")
         assert cp.get_status(table) == cp.CP_OK
         e = entry(w, idx.numel(), float(np.median(t)))
         e["calls_per_step"] = 2
@@ -797,9 +799,9 @@ def host_path_measure(args, w, idx, flush, stream):
     # access path); the larger of the two is the roofline
     dst = stage[: 1 << 30]
     src = host[: 1 << 30]
-    th = time_steps(lambda: dst.copy_(src, non_blocking=True), 10, 2, flush, stream)
+    th = time_steps(lambda: dst.copy_(src, non_blocking=True), 10, 2, flush, stream, "link")
     h2d = (1 << 30) / float(np.median(th)) / 1e9
-    tz = time_steps(lambda: cp.measure_stream_read(src, stream), 10, 2, flush, stream)
+    tz = time_steps(lambda: cp.measure_stream_read(src, stream), 10, 2, flush, stream, "link")
     zero_copy = (1 << 30) / float(np.median(tz)) / 1e9
     link = max(h2d, zero_copy)
     link_kind = ("zero-copy streaming read of 1 GB pinned (cp_measure_stream_read)"
@@ -809,7 +811,8 @@ def host_path_measure(args, w, idx, flush, stream):
     n = idx.numel()
     out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
     hsteps = min(args.steps, 50) if args.only == "host" else 50
-    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), hsteps, 3, flush, stream)
+    t = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), hsteps, 3, flush, stream,
+                   "host")
     assert cp.get_status(table) == cp.CP_OK
     tm = float(np.median(t))
     link_gbs = n * R / tm / 1e9
@@ -820,7 +823,7 @@ def host_path_measure(args, w, idx, flush, stream):
         hot = synth.feistel_bijection(np.arange(1 << 20), w.n_rows, synth.SEED_INDEX)
         cp.set_cache(table, hot)
         tc = time_steps(lambda: cp.lookup_decode_host(table, idx, out, stream), hsteps, 3, flush,
-                        stream)
+                        stream, "host_cached")
         assert cp.get_status(table) == cp.CP_OK
         tcm = float(np.median(tc))
         cached = {"hot_rows": 1 << 20, "cache_bytes": (1 << 20) * R, "ms_per_step": tcm * 1e3,

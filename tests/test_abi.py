@@ -117,3 +117,14 @@ def test_wrappers_reject_short_record_buffers(cplib):
     with pytest.raises(ValueError):
         cp.load_table(full, n_rows, d, k, layout=cp.CP_LAYOUT_SOA,
                       soa=torch.zeros(cp.soa_bytes(n_rows, d, k) - 16, dtype=torch.uint8))
+
+
+def test_stream_read_argument_checks_on_host(cplib):
+    """Null, misaligned or ragged buffers are refused before any CUDA call."""
+    import ctypes
+    buf = (ctypes.c_uint8 * 64)()
+    base = (ctypes.addressof(buf) + 15) & ~15
+    assert cplib.cp_measure_stream_read(None, 16, None) == 1
+    assert cplib.cp_measure_stream_read(base + 4, 16, None) == 1
+    assert cplib.cp_measure_stream_read(base, 0, None) == 1
+    assert cplib.cp_measure_stream_read(base, 24, None) == 1

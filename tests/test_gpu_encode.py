@@ -72,3 +72,26 @@ def test_encoder_more_rows_than_clusters():
 def test_encoder_rejects_bad_geometry():
     with pytest.raises(cp.CPError):
         cp.encode_rows(torch.zeros((2, 8), device="cuda"), 4)      # d < 16
+
+
+def test_encoder_with_caller_workspace_matches():
+    """cp_encode_rows_ws (caller-owned workspace, queue-only) gives the records and
+    costs of cp_encode_rows, reuses one workspace across calls, and rejects a
+    workspace smaller than cp_encode_workspace_bytes."""
+    d, k, rows = 128, 5, 20
+    e = torch.from_numpy(synth.normal_rows(71, rows, d).astype(np.float32)).cuda()
+    ref, ref_cost = cp.encode_rows(e, k)
+    ws = cp.encode_workspace(rows, d, k)
+    for _ in range(2):
+        rec = torch.empty_like(ref)
+        cost = torch.empty_like(ref_cost)
+        cp.encode_rows_ws(e, k, ws, rec, cost)
+        torch.cuda.synchronize()
+        assert torch.equal(rec, ref)
+        assert torch.equal(cost.view(torch.int32), ref_cost.view(torch.int32))
+    L = cp.lib()
+    lut = cp.default_lut()
+    small = ws[: ws.numel() - 256]
+    rc = L.cp_encode_rows_ws(e.data_ptr(), rows, d, k, lut.ctypes.data, rec.data_ptr(), None,
+                             small.data_ptr(), small.numel(), None)
+    assert rc == cp.CP_ERR_INVALID_ARG

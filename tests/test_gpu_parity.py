@@ -368,3 +368,17 @@ def test_cuda_graph_capture_and_replay(lut):
     assert cp.get_status(table) == cp.CP_OK and cp.get_status(htable) == cp.CP_OK
     table.close()
     htable.close()
+
+
+@pytest.mark.parametrize("n_rows", [1, 2, 5, 4097])
+def test_host_resident_tiny_tables(lut, n_rows):
+    """Host-resident tables with one or a few row ranges (the partition's edge cases)."""
+    d, k, n = 512, 4, 3001
+    rec_cpu = synth.gen_records(SEED, torch.arange(n_rows), d, k).reshape(-1).contiguous()
+    table = cp.load_table(rec_cpu.pin_memory(), n_rows, d, k, lut)
+    idx = synth.uniform_indices(n_rows, n, n_rows)
+    idx[::97] = n_rows                                    # out of range: zero rows
+    got = _run(table, idx, layout_host=True).reshape(n, d)
+    assert cp.get_status(table) == cp.CP_ERR_INDEX_OOB
+    _assert_exact(got, oracle_decode(SEED, d, k, idx, n_rows, lut), f"host n_rows={n_rows}")
+    table.close()

@@ -89,7 +89,7 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   if (!host_path) {
     // Non-persistent grid: kBlkWarps * block_rows(ci) lookups per CTA.
     const int rows = cpk::block_rows(ci);
-    const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::kLutRepBlock)) +
+    const size_t smem = static_cast<size_t>(cpk::lut_bytes(cpk::block_rep(ci))) +
                         static_cast<size_t>(cpk::kBlkWarps) * rows * p.stage_bytes;
     if (smem > static_cast<size_t>(t->max_smem)) {
       g_last_error = "geometry needs more shared memory than the device offers";

@@ -10,9 +10,8 @@
 //
 // Repeated ids (about half of a Zipf replay's lookups) are visited like any
 // other: the lookups of one id fall into the same range and so into the same
-// stretch of the visiting order, and the records of a whole replay fit in L2,
-// so a repeat reads its record from L2 and only the first read crosses the host
-// link.  Ids named in a hot-row cache (frequency-based caching) keep their
+// slice of the visiting order, which one SM decodes, so a repeat mostly finds
+// the record in that SM's L1 cache.  (Host-memory reads are not kept in L2.)  Ids named in a hot-row cache (frequency-based caching) keep their
 // place in that order and read their record from its HBM copy, so every warp
 // mixes link reads with cache reads.
 #include <cstdint>

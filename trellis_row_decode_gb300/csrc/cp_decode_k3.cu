@@ -19,8 +19,8 @@ void fill(DecodeFn* row) {
 template <bool SOA>
 void fill_block(DecodeFn* row) {
   row[0] = &lookup_decode_block_kernel<3, SOA, 0, kLutRepBlock, kBlkRows>;
-  row[1] = &lookup_decode_block_kernel<3, SOA, 1, kLutRepBlock, block_rows(1)>;
-  row[2] = &lookup_decode_block_kernel<3, SOA, 2, kLutRepBlock, block_rows(2)>;
+  row[1] = &lookup_decode_block_kernel<3, SOA, 1, block_rep(1), block_rows(1)>;
+  row[2] = &lookup_decode_block_kernel<3, SOA, 2, block_rep(2), block_rows(2)>;
   row[3] = &lookup_decode_block_kernel<3, SOA, 4, kLutRepBlock, kBlkRows>;
   row[4] = &lookup_decode_block_kernel<3, SOA, 8, kLutRepBlock, kBlkRows>;
   row[5] = &lookup_decode_block_kernel<3, SOA, 16, kLutRepBlock, kBlkRows>;

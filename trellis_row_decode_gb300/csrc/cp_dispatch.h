@@ -46,6 +46,13 @@ constexpr int kBlkRowsShort = CP_BLK_ROWS_SHORT;
 constexpr int block_rows(int cpl_idx) {
   return (cpl_idx == 1 || cpl_idx == 2) ? kBlkRowsShort : kBlkRows;
 }
+// LUT replicas of the HBM block kernel per chunks-per-lane index: one where a
+// warp decodes several short rows per step (the fill per row written weighs more:
+// d = 512 table 0.0402 -> 0.0390 ms), kLutRepBlock elsewhere (d = 1024: 1 and 2
+// replicas are within noise).
+constexpr int block_rep(int cpl_idx) {
+  return (cpl_idx == 1 || cpl_idx == 2) ? 1 : kLutRepBlock;
+}
 
 inline int cpl_index(uint32_t d) {
   for (int i = 1; i < kCplVariants; ++i)
@@ -68,12 +75,18 @@ constexpr int kPfReduce = CP_PF_REDUCE;
 // Host-path kernels for cpl indices 1..3 are lookup_decode_host_kernel (one
 // shared stage per warp, kHostWarps warps per CTA).
 inline bool host_uses_register_ring(int cpl_idx) { return cpl_idx >= 1 && cpl_idx <= 3; }
-constexpr int kPfHostReg = 8;
+#ifndef CP_PF_HOST_REG
+#define CP_PF_HOST_REG 4
+#endif
+constexpr int kPfHostReg = CP_PF_HOST_REG;
 
 
 // Host-resident tables: lookups are visited bucketed by row-id range so that
 // consecutive records of a warp are close in the host address space.
-constexpr uint32_t kBucketBits = 12;                  // 4096 ranges (cpx::kBucketBitsHost)
+#ifndef CP_BUCKET_BITS
+#define CP_BUCKET_BITS 12
+#endif
+constexpr uint32_t kBucketBits = CP_BUCKET_BITS;      // 4096 ranges (cpx::kBucketBitsHost)
 constexpr uint32_t kBucketChunk = 1u << 20;           // lookups per pass
 
 // Hot-row cache construction: records of the m rows `rows` (device ids, sorted)

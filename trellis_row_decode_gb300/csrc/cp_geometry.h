@@ -9,7 +9,10 @@ namespace cpx {
 
 constexpr uint64_t kMaxRows = 1ull << 40;
 constexpr uint64_t kMaxLookups = 1ull << 40;
-constexpr uint32_t kBucketBitsHost = 12;              // at most 2^12 row ranges
+#ifndef CP_BUCKET_BITS
+#define CP_BUCKET_BITS 12
+#endif
+constexpr uint32_t kBucketBitsHost = CP_BUCKET_BITS;  // at most 2^12 row ranges
 
 // Geometry accepted by the CUDA path: k in {3,..,6}, d % 8 == 0 in [8, 4096],
 // and a whole number of 16-bit words per record (so every record starts

@@ -423,6 +423,17 @@ def hbm_same_run(flush, stream, steps: int = 20):
                     f"{steps}, L2 flushed between"}
 
 
+def d2h_link_gbs(flush, stream) -> float:
+    """Device-to-host link rate in this run: 1 GB copies to pinned memory (the bound of
+    the e2e step, which moves every row to the host)."""
+    import torch
+    src = torch.ones(1 << 30, dtype=torch.uint8, device="cuda")
+    dst = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    t = time_steps(lambda: dst.copy_(src, non_blocking=True), 10, 2, flush, stream, "link")
+    del src, dst
+    return (1 << 30) / float(np.median(t)) / 1e9
+
+
 def aggregate(local_time_s: float, local_units: int, world: int, dist, device):
     """Max of the ranks' timed totals and the whole-job throughput.
 
@@ -509,6 +520,7 @@ def our_arm(args, w, rank, world, local):
 
     te = time_steps(e2e_step, args.e2e_steps, 3, flush, stream, "e2e")
     _, e2e_value = aggregate(float(te.sum()), n * args.e2e_steps, world, dist, "cuda")
+    d2h = d2h_link_gbs(flush, stream) if solo else None
 
     host_obj = None
     if not args.no_host_path and solo and w.residency in ("device", "host") \
@@ -547,7 +559,11 @@ def our_arm(args, w, rank, world, local):
                          "bytes_per_lookup": bpl, "kernel": "lookup_decode_block_kernel"},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": n * 8,
                     "path": "ids copied from pinned host memory; rows written by the decode kernel into pinned host memory",
-                    "d2h_bytes_per_step": n * w.d * 2},
+                    "d2h_bytes_per_step": n * w.d * 2,
+                    **({"d2h_link_gbs": d2h,
+                        "frac_of_d2h_link": n * w.d * 2 * e2e_value / n / 1e9 / d2h,
+                        "d2h_link_kind": "measured: cudaMemcpyAsync device->pinned, 1 GB"}
+                       if d2h else {})},
             "gpu_launches": args.steps,
             "clocks": clk,
             "step_ms": {"min": float(t.min() * 1e3), "median": float(np.median(t) * 1e3),

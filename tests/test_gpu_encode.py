@@ -42,10 +42,11 @@ def test_encoder_round_trip_through_decode():
     assert mse < rtn and mse < 0.1175
 
 
-@pytest.mark.parametrize("d,k", [(16, 4), (16, 6), (1024, 4), (1024, 3), (1024, 6), (4096, 3)])
+@pytest.mark.parametrize("d,k", [(16, 4), (16, 6), (32, 3), (1024, 4), (1024, 3), (1024, 5),
+                                 (1024, 6), (4096, 3), (4096, 6)])
 def test_encoder_edge_and_large_rows(d, k):
-    """Smallest rows (T = 8 steps), the d = 1024 tables, and the largest row with
-    the largest group-minimum buffers (k = 3): records and costs bit for bit."""
+    """Smallest rows (T = 8 steps), the d = 1024 tables at every k, and the largest
+    rows (k = 3 has the largest group-minimum buffers): records and costs bit for bit."""
     rows = 40 if d <= 16 else 6
     e = synth.normal_rows(7 + d + k, rows, d).astype(np.float32)
     e[1] = 0.0
@@ -58,9 +59,10 @@ def test_encoder_edge_and_large_rows(d, k):
     assert np.array_equal(cost.cpu().numpy().view(np.uint32), ref_cost.view(np.uint32))
 
 
-def test_encoder_more_rows_than_clusters():
+@pytest.mark.parametrize("k", [3, 4, 6])
+def test_encoder_more_rows_than_clusters(k):
     """Several rows per cluster (the persistent loop), d = 64."""
-    d, k, rows = 64, 4, 300
+    d, rows = 64, 300
     e = synth.normal_rows(77, rows, d).astype(np.float32)
     rec, cost = cp.encode_rows(torch.from_numpy(e).cuda(), k)
     torch.cuda.synchronize()

@@ -107,8 +107,12 @@ __global__ void __launch_bounds__(kBlkWarps * 32)
       const int64_t r = __ldg(p.idx + j);
       if (static_cast<uint64_t>(r) < p.n_rows) {
         const uint64_t o0 = __ldg(offsets + r);
-        const uint64_t k = (__ldg(offsets + r + 1) - o0 - 2) * 16 / d;
-        my_loc = (o0 << 4) | ((k - 3) << 1) | 1u;
+        // code bytes c = d k / 16 with k in {3, .., 6} (checked at load), so 16 c
+        // = k d: k - 3 by three comparisons (a 64-bit division by the runtime d
+        // cost the warp a long instruction sequence per row group)
+        const uint32_t c16 = static_cast<uint32_t>(__ldg(offsets + r + 1) - o0 - 2) * 16;
+        const uint32_t k3 = (c16 > 3 * d) + (c16 > 4 * d) + (c16 > 5 * d);
+        my_loc = (o0 << 4) | (static_cast<uint64_t>(k3) << 1) | 1u;
       } else {
         atomicOr(p.status, 1u);
       }

@@ -823,6 +823,12 @@ def host_path_measure(args, w, idx, flush, stream):
     link_kind = ("zero-copy streaming read of 1 GB pinned (cp_measure_stream_read)"
                  if zero_copy >= h2d else "cudaMemcpyAsync pinned->device, 1 GB")
     del stage, dst
+    # the access pattern's own roofline: the replay's distinct records, sorted, read
+    # once each over the link as the 16-byte pieces that cover them (no decode)
+    uq_rows = torch.unique(idx)
+    tr = time_steps(lambda: cp.measure_record_read(host, R, uq_rows, stream), 10, 2, flush, stream,
+                    "link")
+    record_read = int(uq_rows.numel()) * R / float(np.median(tr)) / 1e9
     table = cp.load_table(host, w.n_rows, w.d, w.k, cp.default_lut())
     n = idx.numel()
     out = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
@@ -856,6 +862,10 @@ def host_path_measure(args, w, idx, flush, stream):
             "unique_ids": uniq, "bytes_per_lookup": R,
             "achieved_unique": uniq * R / tm / 1e9,
             "link_frac_unique": uniq * R / tm / 1e9 / link,
+            "record_read_gbs": record_read,
+            "record_read_kind": "measured: cp_measure_record_read of the replay's distinct ids, "
+                                "sorted, no decode (record bytes / time)",
+            "frac_of_record_read": uniq * R / tm / 1e9 / record_read,
             "achieved_lookup_bytes": link_gbs,
             "frac_lookup_bytes": link_gbs / link,
             "note": "link_frac_unique counts the records that cross the link (one per distinct "

@@ -168,10 +168,10 @@ cp_status cp_lookup_decode(const cp_table* t, const int64_t* idx, uint64_t n, ui
  * grouped by row-id range (a counting partition into 4096 ranges), so that
  * successive host reads are close in the host address space; every row is still
  * written at its own position.  Each SM takes one contiguous slice of that
- * order; the repeats of an id fall into the same slice and mostly find the
- * record in that SM's L1 cache (on a 196,608-lookup Zipf replay, about 1.16
- * fetches per distinct id cross the host link, against 2.2 for one fetch per
- * lookup).  This state lives in 8.4 MB of device scratch owned by
+ * order; the repeats of an id fall into the same slice and find the record in
+ * that SM's L1 cache (on a 196,608-lookup Zipf replay, about 1.03 fetches per
+ * distinct id cross the host link, against 2.2 for one fetch per lookup).
+ * This state lives in 8.4 MB of device scratch owned by
  * the handle (allocated by cp_table_load), so calls on one host-resident handle
  * must be ordered on one stream (or otherwise serialised).
  */
@@ -329,6 +329,26 @@ cp_status cp_lookup_decode_host_noalloc(const void* records, uint64_t n_rows, ui
  * CP_ERR_INVALID_ARG for any other buffer; queues one kernel, no allocation.
  */
 cp_status cp_measure_stream_read(const void* buf, uint64_t bytes, void* stream);
+
+/*
+ * cp_measure_record_read -- read the records rows[0..n) of a record table once,
+ * each as the 16-byte pieces that cover it (the host path's own loads), with no
+ * decode and nothing observable written.  Timed with events on `stream` with
+ * the distinct ids of a replay, sorted, it gives the rate at which the host link
+ * delivers whole records at scattered addresses: the roofline of
+ * cp_lookup_decode_host's access pattern, below the streaming rate because a
+ * 258-byte record at a 2-byte boundary spans nine 32-byte sectors.  The pages
+ * place the table in pinned host DRAM as the slow placement [P4 "assumptions
+ * and limits"]; this measures that placement's record rate on the machine.
+ *   table         device memory or mapped page-locked host memory, 16-byte
+ *                 aligned, table_bytes long (at least one record).
+ *   record_bytes  bytes per record (R); record r starts at byte r * R.
+ *   rows, n       device array of n > 0 int64 row ids, 8-byte aligned; ids at or
+ *                 past table_bytes / R are skipped.
+ * CP_ERR_INVALID_ARG for any other argument; queues one kernel, no allocation.
+ */
+cp_status cp_measure_record_read(const void* table, uint64_t table_bytes, uint32_t record_bytes,
+                                 const int64_t* rows, uint64_t n, void* stream);
 
 /* Release what the handle owns (LUT copy, status word, host registration made
  * by cp_table_load).  Borrowed buffers are untouched.  NULL is a no-op. */

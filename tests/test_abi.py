@@ -128,3 +128,24 @@ def test_stream_read_argument_checks_on_host(cplib):
     assert cplib.cp_measure_stream_read(base + 4, 16, None) == 1
     assert cplib.cp_measure_stream_read(base, 0, None) == 1
     assert cplib.cp_measure_stream_read(base, 24, None) == 1
+
+
+def test_record_read_argument_checks_on_host(cplib):
+    """Null or misaligned buffers, no rows, a zero or oversized record are refused
+    before any CUDA call."""
+    import ctypes
+    f = cplib.cp_measure_record_read
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p,
+                  ctypes.c_uint64, ctypes.c_void_p]
+    buf = (ctypes.c_uint8 * 1024)()
+    base = (ctypes.addressof(buf) + 15) & ~15
+    rows = (ctypes.c_int64 * 4)()
+    r = ctypes.addressof(rows)
+    assert f(None, 512, 258, r, 1, None) == 1
+    assert f(base, 512, 258, None, 1, None) == 1
+    assert f(base, 512, 0, r, 1, None) == 1
+    assert f(base, 512, 258, r, 0, None) == 1
+    assert f(base, 100, 258, r, 1, None) == 1
+    assert f(base + 4, 512, 258, r, 1, None) == 1
+    assert f(base, 512, 258, r + 4, 1, None) == 1

@@ -23,7 +23,7 @@ __all__ = [
     "CPError", "Table", "load_table", "lookup_decode", "lookup_decode_host", "get_status",
     "record_bytes", "soa_bytes", "default_lut", "lib", "LIB_PATH", "lookup_decode_host_noalloc",
     "lookup_decode_reduce", "set_cache", "load_mixed_table", "encode_rows",
-    "measure_stream_read", "encode_workspace", "encode_rows_ws",
+    "measure_stream_read", "measure_record_read", "encode_workspace", "encode_rows_ws",
     "CP_LAYOUT_AOS", "CP_LAYOUT_SOA", "CP_RESIDENT_DEVICE", "CP_RESIDENT_HOST",
 ]
 
@@ -91,6 +91,8 @@ def lib():
         L.cp_encode_rows_ws.argtypes = [vp, u64, u32, u32, vp, vp, vp, vp, u64, vp]
         L.cp_measure_stream_read.restype = i32
         L.cp_measure_stream_read.argtypes = [vp, u64, vp]
+        L.cp_measure_record_read.restype = i32
+        L.cp_measure_record_read.argtypes = [vp, u64, u32, vp, u64, vp]
         _lib = L
     return _lib
 
@@ -299,6 +301,20 @@ def measure_stream_read(buf: torch.Tensor, stream=None) -> None:
         raise ValueError("buf must be contiguous with a size that is a multiple of 16 bytes")
     _check(lib().cp_measure_stream_read(buf.data_ptr(), buf.numel() * buf.element_size(),
                                         _stream_ptr(stream)), "cp_measure_stream_read")
+
+
+def measure_record_read(table: torch.Tensor, record_bytes: int, rows: torch.Tensor,
+                        stream=None) -> None:
+    """Queue one read of the records `rows` (device int64) of `table` (a record
+    table in device memory or pinned host memory, R = record_bytes per row), each
+    as the 16-byte pieces that cover it; time it with events on `stream`."""
+    if not table.is_contiguous() or not rows.is_contiguous() or rows.dtype != torch.int64:
+        raise ValueError("table must be contiguous and rows a contiguous int64 tensor")
+    if not rows.is_cuda:
+        raise ValueError("rows must be in device memory")
+    _check(lib().cp_measure_record_read(table.data_ptr(), table.numel() * table.element_size(),
+                                        record_bytes, rows.data_ptr(), rows.numel(),
+                                        _stream_ptr(stream)), "cp_measure_record_read")
 
 
 def encode_workspace(rows: int, d: int, k: int) -> torch.Tensor:

@@ -115,7 +115,7 @@ cp_status launch_decode(const cp_table* t, const int64_t* idx, uint64_t n, uint1
   const int pf = cpk::kPfHost;
   const bool reg_ring = cpk::host_uses_register_ring(ci);
   int nwarps = reg_ring ? cpk::kHostWarps : cpk::kMaxWarps;
-  const size_t lut = cpk::lut_bytes(reg_ring ? 32 : cpk::kLutRepHost);
+  const size_t lut = cpk::lut_bytes(reg_ring ? cpk::kLutRepHostReg : cpk::kLutRepHost);
   auto smem_for = [&](int w) {
     if (reg_ring) return lut + static_cast<size_t>(w) * p.stage_bytes;   // one stage per warp
     return lut + static_cast<size_t>(w) * pf * p.stage_bytes + static_cast<size_t>(w) * pf * 8;

@@ -33,12 +33,12 @@ KernelSet kernels_k4() {
   fill_block<true>(s.dev[1]);
   fill<false, kPfHost, true, kLutRepHost>(s.host[0]);
   fill<true, kPfHost, true, kLutRepHost>(s.host[1]);
-  s.host[0][1] = &lookup_decode_host_kernel<4, false, kPfHostReg, 1, 32>;
-  s.host[0][2] = &lookup_decode_host_kernel<4, false, kPfHostReg, 2, 32>;
-  s.host[0][3] = &lookup_decode_host_kernel<4, false, kPfHostReg, 4, 32>;
-  s.host[1][1] = &lookup_decode_host_kernel<4, true, kPfHostReg, 1, 32>;
-  s.host[1][2] = &lookup_decode_host_kernel<4, true, kPfHostReg, 2, 32>;
-  s.host[1][3] = &lookup_decode_host_kernel<4, true, kPfHostReg, 4, 32>;
+  s.host[0][1] = &lookup_decode_host_kernel<4, false, kPfHostReg, 1, kLutRepHostReg>;
+  s.host[0][2] = &lookup_decode_host_kernel<4, false, kPfHostReg, 2, kLutRepHostReg>;
+  s.host[0][3] = &lookup_decode_host_kernel<4, false, kPfHostReg, 4, kLutRepHostReg>;
+  s.host[1][1] = &lookup_decode_host_kernel<4, true, kPfHostReg, 1, kLutRepHostReg>;
+  s.host[1][2] = &lookup_decode_host_kernel<4, true, kPfHostReg, 2, kLutRepHostReg>;
+  s.host[1][3] = &lookup_decode_host_kernel<4, true, kPfHostReg, 4, kLutRepHostReg>;
   s.reduce[0][0] = &lookup_decode_reduce_kernel<4, false, kPfReduce, 1>;
   s.reduce[0][1] = &lookup_decode_reduce_kernel<4, false, kPfReduce, 2>;
   s.reduce[0][2] = &lookup_decode_reduce_kernel<4, false, kPfReduce, 4>;

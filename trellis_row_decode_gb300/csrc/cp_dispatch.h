@@ -79,6 +79,12 @@ inline bool host_uses_register_ring(int cpl_idx) { return cpl_idx >= 1 && cpl_id
 #define CP_PF_HOST_REG 4
 #endif
 constexpr int kPfHostReg = CP_PF_HOST_REG;
+// LUT replicas of the register-ring kernel.  The kernel waits on the host link,
+// not on LUT bank conflicts, and what shared memory it does not take is L1 that
+// holds the records repeats read: 4 replicas (16 KB) against 32 (128 KB) took the
+// 2^24-row d = 1024 table from 0.208 to 0.189 ms and the 51 GB one from 0.230
+// to 0.215 ms (8 and 16 replicas fall in between).
+constexpr int kLutRepHostReg = 4;
 
 
 // Host-resident tables: lookups are visited bucketed by row-id range so that
@@ -98,10 +104,10 @@ void launch_cache_build(const uint8_t* table, uint32_t R, const int64_t* rows, u
 
 // Visiting order of n lookups for a host-resident table: perm = the lookups
 // grouped by range (id >> shift; range nb: ids outside [0, n_rows)), a counting
-// partition (count, scan, scatter).  With a cache map (cmap_ts > 0) cslot[j]
-// receives the cache slot of idx[j] or 0xFFFFFFFF.  counts (nb + 1 words) must
-// hold zeros on entry and holds zeros again afterwards; cursor (nb + 1 words)
-// is scratch.
+// partition (count with the scan in its last CTA, then scatter).  With a cache
+// map (cmap_ts > 0) cslot[j] receives the cache slot of idx[j] or 0xFFFFFFFF.
+// counts (nb + 2 words: the counts and a completion ticket) must hold zeros on
+// entry and holds zeros again afterwards; cursor (nb + 1 words) is scratch.
 void launch_bucket_partition(const int64_t* idx, uint64_t n, uint64_t n_rows,
                              const unsigned long long* cmap_keys, const uint32_t* cmap_vals,
                              uint32_t cmap_ts, uint32_t* cslot, uint32_t shift, uint32_t nb,

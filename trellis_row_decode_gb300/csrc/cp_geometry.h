@@ -40,8 +40,9 @@ inline void bucket_params(uint64_t n_rows, uint32_t* shift, uint32_t* nb) {
   *nb = static_cast<uint32_t>(((n_rows - 1) >> *shift) + 1);
 }
 
-// Words of one per-range array (nb + 1 ranges, padded to 64 words).
-constexpr size_t host_scratch_count_words(uint32_t nb) { return (nb + 1 + 63) & ~63u; }
+// Words of one per-range array (nb + 1 ranges and one more word, the counts'
+// completion ticket, padded to 64 words).
+constexpr size_t host_scratch_count_words(uint32_t nb) { return (nb + 2 + 63) & ~63u; }
 
 // Device scratch of the host path for passes of `capacity` lookups: range
 // counts and cursors, then the visiting order and the cache slot per lookup.

@@ -44,6 +44,7 @@ template <int K, bool SOA, int PF, int CPL, int REP>
 __global__ void __launch_bounds__(kHostWarps * 32, 1)
     lookup_decode_host_kernel(const DecodeParams p) {
   static_assert(CPL >= 1 && CPL <= 4, "one 16-byte piece per lane");
+  static_assert(REP >= 4 && REP % 4 == 0, "the LUT fill writes 16-byte groups of replicas");
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31;

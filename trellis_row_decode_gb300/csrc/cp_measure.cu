@@ -1,6 +1,7 @@
-// cp_measure.cu -- streaming-read kernel that measures the bandwidth bounding a
-// lookup-decode: over the host link for a pinned host buffer read zero-copy (the
-// roofline of cp_lookup_decode_host), or from HBM for a device buffer.
+// cp_measure.cu -- read kernels that measure the bandwidth bounding a
+// lookup-decode: a streaming read over the host link for a pinned host buffer
+// read zero-copy (or from HBM for a device buffer), and a read of scattered
+// whole records, the host path's own access pattern without its decode.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -43,22 +44,92 @@ __global__ void __launch_bounds__(256) stream_read_kernel(const uint4* __restric
   if (acc == 0x9E3779B9u) g_measure_sink = acc;
 }
 
+// Each listed record read once as the 16-byte pieces that cover it (the host
+// path's loads), one CTA per SM taking a contiguous slice of the list, each warp
+// four records in flight; pieces that would reach past the table are skipped.
+__global__ void __launch_bounds__(1024, 1)
+    record_read_kernel(const uint8_t* __restrict__ table, uint64_t table_bytes, uint32_t R,
+                       const int64_t* __restrict__ rows, uint64_t n) {
+  constexpr int kInFlight = 4;
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const uint64_t lo = static_cast<uint64_t>(blockIdx.x) * n / gridDim.x;
+  const uint64_t hi = static_cast<uint64_t>(blockIdx.x + 1) * n / gridDim.x;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(table);
+  uint32_t acc = 0;
+  for (uint64_t q = lo + warp; q < hi; q += static_cast<uint64_t>(nw) * kInFlight) {
+    uint4 v[kInFlight];
+#pragma unroll
+    for (int s = 0; s < kInFlight; ++s) {
+      v[s] = make_uint4(0, 0, 0, 0);
+      const uint64_t qq = q + static_cast<uint64_t>(s) * nw;
+      if (qq < hi) {
+        const uint64_t r = static_cast<uint64_t>(__ldg(rows + qq));
+        const uint64_t off = r * R;
+        if (r < table_bytes / R) {
+          const uint64_t o0 = off & ~static_cast<uint64_t>(15);
+          const uint32_t nch = static_cast<uint32_t>(off - o0 + R + 15) >> 4;
+          const uint64_t po = o0 + 16u * lane;
+          if (lane < nch && po + 16 <= table_bytes) v[s] = ld_stream(reinterpret_cast<const uint4*>(base + po));
+        }
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < kInFlight; ++s) acc ^= v[s].x ^ v[s].y ^ v[s].z ^ v[s].w;
+  }
+  if (acc == 0x9E3779B9u) g_measure_sink = acc;
+}
+
+// Device address of buf: itself for device memory, its alias for mapped
+// page-locked host memory, nullptr otherwise.
+const void* device_view(const void* buf, cudaError_t* err) {
+  cudaPointerAttributes attr{};
+  *err = cudaPointerGetAttributes(&attr, buf);
+  if (*err != cudaSuccess) return nullptr;
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) return buf;
+  if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) return attr.devicePointer;
+  return nullptr;
+}
+
 }  // namespace
+
+extern "C" cp_status cp_measure_record_read(const void* table, uint64_t table_bytes,
+                                            uint32_t record_bytes, const int64_t* rows,
+                                            uint64_t n, void* stream) {
+  if (table == nullptr || rows == nullptr || record_bytes == 0 || n == 0 ||
+      table_bytes < record_bytes || !cpx::aligned(table, 16) || !cpx::aligned(rows, 8)) {
+    cpx::set_error("table and rows must be non-null (16- and 8-byte aligned), n and record_bytes "
+                   "positive, table_bytes at least one record");
+    return CP_ERR_INVALID_ARG;
+  }
+  cudaError_t e = cudaSuccess;
+  const void* dptr = device_view(table, &e);
+  if (e != cudaSuccess) return cpx::cuda_fail(e, "cudaPointerGetAttributes");
+  if (dptr == nullptr) {
+    cpx::set_error("table is neither device memory nor mapped page-locked host memory");
+    return CP_ERR_INVALID_ARG;
+  }
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cpx::cuda_fail(e, "device query");
+  uint64_t blocks = static_cast<uint64_t>(sms);
+  if (blocks > n) blocks = n;
+  record_read_kernel<<<static_cast<unsigned>(blocks), 1024, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(dptr), table_bytes, record_bytes, rows, n);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cpx::cuda_fail(e, "record-read launch");
+  return CP_OK;
+}
 
 extern "C" cp_status cp_measure_stream_read(const void* buf, uint64_t bytes, void* stream) {
   if (buf == nullptr || bytes == 0 || (bytes % 16) != 0 || !cpx::aligned(buf, 16)) {
     cpx::set_error("buffer must be non-null and 16-byte aligned, bytes a positive multiple of 16");
     return CP_ERR_INVALID_ARG;
   }
-  cudaPointerAttributes attr{};
-  cudaError_t e = cudaPointerGetAttributes(&attr, buf);
+  cudaError_t e = cudaSuccess;
+  const void* dptr = device_view(buf, &e);
   if (e != cudaSuccess) return cpx::cuda_fail(e, "cudaPointerGetAttributes");
-  const void* dptr = nullptr;
-  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
-    dptr = buf;
-  } else if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) {
-    dptr = attr.devicePointer;                  // device alias of page-locked host memory
-  } else {
+  if (dptr == nullptr) {
     cpx::set_error("buffer is neither device memory nor mapped page-locked host memory");
     return CP_ERR_INVALID_ARG;
   }

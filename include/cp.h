@@ -300,9 +300,8 @@ cp_status cp_get_status(const cp_table* t, void* stream);
  * library holds until the process exits.  Limit: n <= 65536 lookups per call;
  * larger n returns CP_ERR_INVALID_ARG before any work is queued.
  * The first call on a device looks up that array's device address and clears
- * its counters with a synchronous memset (once per device); make that first call
- * before any stream capture.  The address is kept
- * for the life of the process: after cudaDeviceReset it no longer names the
+ * its counters with a synchronous memset (once per device, so that first call
+ * synchronises the device).  The address is kept for the life of the process: after cudaDeviceReset it no longer names the
  * array, so do not call this entry point on a device that has been reset.  All calls share the
  * array and it keeps the last call's contents (each call clears what must start
  * empty), so calls that overlap on the GPU (on different streams, or from

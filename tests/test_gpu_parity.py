@@ -382,3 +382,27 @@ def test_host_resident_tiny_tables(lut, n_rows):
     assert cp.get_status(table) == cp.CP_ERR_INDEX_OOB
     _assert_exact(got, oracle_decode(SEED, d, k, idx, n_rows, lut), f"host n_rows={n_rows}")
     table.close()
+
+
+@pytest.mark.parametrize("pattern", ["one_id", "dominant_id", "sorted", "reversed"])
+def test_host_resident_skewed_ids(lut, pattern):
+    """Lookup streams that load the partition unevenly, over many partition CTAs
+    (2,048 lookups each): every lookup on one id (one range takes every rank), a
+    dominant id mixed with uniform ids, and ids in ascending or descending order
+    (each CTA's lookups in one or two ranges).  Every element against the oracle."""
+    d, k, n_rows, n = 256, 4, 70001, 100003
+    rec_cpu = synth.gen_records(SEED, torch.arange(n_rows), d, k).reshape(-1).contiguous()
+    table = cp.load_table(rec_cpu.pin_memory(), n_rows, d, k, lut)
+    idx = synth.uniform_indices(21, n, n_rows)
+    if pattern == "one_id":
+        idx[:] = 4321
+    elif pattern == "dominant_id":
+        idx[::2] = n_rows - 1                           # the last record, half the lookups
+    elif pattern == "sorted":
+        idx.sort()
+    else:
+        idx[::-1].sort()
+    got = _run(table, idx, layout_host=True).reshape(n, d)
+    assert cp.get_status(table) == cp.CP_OK
+    _assert_exact(got, oracle_decode(SEED, d, k, idx, n_rows, lut), f"host {pattern}")
+    table.close()

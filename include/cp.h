@@ -342,8 +342,8 @@ cp_status cp_measure_stream_read(const void* buf, uint64_t bytes, void* stream);
  *   table         device memory or mapped page-locked host memory, 16-byte
  *                 aligned, table_bytes long (at least one record).
  *   record_bytes  bytes per record (R); record r starts at byte r * R.
- *   rows, n       device array of n > 0 int64 row ids, 8-byte aligned; ids at or
- *                 past table_bytes / R are skipped.
+ *   rows, n       device array of n int64 row ids (0 < n < 2^48), 8-byte
+ *                 aligned; ids at or past table_bytes / R are skipped.
  * CP_ERR_INVALID_ARG for any other argument; queues one kernel, no allocation.
  */
 cp_status cp_measure_record_read(const void* table, uint64_t table_bytes, uint32_t record_bytes,

@@ -149,3 +149,4 @@ def test_record_read_argument_checks_on_host(cplib):
     assert f(base, 100, 258, r, 1, None) == 1
     assert f(base + 4, 512, 258, r, 1, None) == 1
     assert f(base, 512, 258, r + 4, 1, None) == 1
+    assert f(base, 512, 258, r, 1 << 48, None) == 1

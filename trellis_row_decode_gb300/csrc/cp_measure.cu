@@ -95,10 +95,10 @@ const void* device_view(const void* buf, cudaError_t* err) {
 extern "C" cp_status cp_measure_record_read(const void* table, uint64_t table_bytes,
                                             uint32_t record_bytes, const int64_t* rows,
                                             uint64_t n, void* stream) {
-  if (table == nullptr || rows == nullptr || record_bytes == 0 || n == 0 ||
+  if (table == nullptr || rows == nullptr || record_bytes == 0 || n == 0 || n >= (1ull << 48) ||
       table_bytes < record_bytes || !cpx::aligned(table, 16) || !cpx::aligned(rows, 8)) {
-    cpx::set_error("table and rows must be non-null (16- and 8-byte aligned), n and record_bytes "
-                   "positive, table_bytes at least one record");
+    cpx::set_error("table and rows must be non-null (16- and 8-byte aligned), n in [1, 2^48), "
+                   "record_bytes positive, table_bytes at least one record");
     return CP_ERR_INVALID_ARG;
   }
   cudaError_t e = cudaSuccess;

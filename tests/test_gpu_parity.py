@@ -406,3 +406,24 @@ def test_host_resident_skewed_ids(lut, pattern):
     assert cp.get_status(table) == cp.CP_OK
     _assert_exact(got, oracle_decode(SEED, d, k, idx, n_rows, lut), f"host {pattern}")
     table.close()
+
+
+@pytest.mark.parametrize("layout", [cp.CP_LAYOUT_AOS, cp.CP_LAYOUT_SOA])
+@pytest.mark.parametrize("d,k", [(16, 6), (64, 4), (256, 3), (512, 5), (2048, 5), (4096, 6),
+                                 (4096, 3)])
+def test_host_resident_small_and_large_rows(lut, d, k, layout):
+    """Host-resident tables outside d = 1024: the register-ring kernel at d = 256
+    and 512, the staged kernel (cp.async ring) for every other d, both layouts; the
+    table's last record is looked up (its reads end at the table's end)."""
+    n_rows, n = 777, 2049
+    rec_cpu = synth.gen_records(SEED + 2, torch.arange(n_rows), d, k).reshape(-1).contiguous()
+    soa = None
+    if layout == cp.CP_LAYOUT_SOA:
+        soa = torch.empty(cp.soa_bytes(n_rows, d, k), dtype=torch.uint8, pin_memory=True)
+    table = cp.load_table(rec_cpu.pin_memory(), n_rows, d, k, lut, layout=layout, soa=soa)
+    idx = synth.uniform_indices(8, n, n_rows)
+    idx[-1] = n_rows - 1
+    got = _run(table, idx, layout_host=True).reshape(n, d)
+    assert cp.get_status(table) == cp.CP_OK
+    _assert_exact(got, oracle_decode(SEED + 2, d, k, idx, n_rows, lut), f"host d={d} k={k}")
+    table.close()

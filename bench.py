@@ -869,7 +869,7 @@ def host_path_measure(args, w, idx, flush, stream):
             "achieved_lookup_bytes": link_gbs,
             "frac_lookup_bytes": link_gbs / link,
             "note": "link_frac_unique counts the records that cross the link (one per distinct "
-                    "id); frac_lookup_bytes counts n * R as the survey's algorithmic bytes"}
+                    "id); frac_lookup_bytes counts n * R, every lookup's record with repeats"}
 
 
 def only_leg(args, w):
